@@ -1,0 +1,170 @@
+/*
+ * muon_gb300.h -- C ABI of the GB300 (sm_103a) Muon optimizer step.
+ *
+ * The Muon step, as the pages describe it:
+ *   [MCS] "Muon Custom Sizing 实战：modded-nanogpt 将注意力与 MLP 参数合并进同一
+ *         reduce_scatter 调用，把 124M GPT 训练压进 150 秒", section 2.3 (batched
+ *         NS of the QKVO view, coefficients (a,b,c) = (3.4445, -4.7750, 2.0315),
+ *         five rounds) and section 四 (momentum lerp, Nesterov blend, decoupled
+ *         decay lr*wd, write-back with alpha = -lr * max(1, hdim/dim)^0.5);
+ *   [PG]  "parameter-golf train_gpt.py 源码精读：Muon 优化器、Int8 量化与 DDP 数据
+ *         加载全解", part 1, section 核心思想 (zeropower_via_newtonschulz5:
+ *         X /= ||X||; repeat A = X X^T, B = bA + cA^2, X = aX + BX) and section
+ *         分布式细节 (rescale g *= max(1, m/n)^0.5).
+ *
+ * Conventions shared by every entry point:
+ *   - Matrices are row-major and contiguous, stacked as [batch, rows, cols].
+ *     A stack of same-shape weights is one call; the [MCS] QKVO weight stored
+ *     as (hdim, 4*dim) is passed as batch 4 of (hdim, dim): the same bytes.
+ *   - Every data pointer is device memory owned by the caller, 16-byte
+ *     aligned.  Parameters and momentum buffers are updated in place;
+ *     gradients are only read.  The library allocates no device memory.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
+ *     work is enqueued on it asynchronously; no entry point synchronises
+ *     except muon_workspace_status().
+ *   - The workspace is caller-owned device memory of at least the size that
+ *     muon_workspace_bytes()/muon_grouped_workspace_bytes() return, 256-byte
+ *     aligned, and zero-filled before its first use (it carries a sticky
+ *     device error word).  Calls that share a workspace must not overlap on
+ *     the GPU.
+ *   - Argument errors are reported before anything is enqueued.  A CUDA error
+ *     while enqueuing gives MUON_ERR_CUDA.  No C++ exception crosses the ABI.
+ *   - NS runs in bf16 on the tensor cores (fp32 accumulation and epilogues)
+ *     for min(rows, cols) >= 64; smaller matrices run the same iteration in
+ *     fp32 on the CUDA cores (bf16 is too coarse for, e.g., a 1x12 gate).
+ *   - When rows > cols the iteration runs on the transpose (A is the
+ *     min(rows,cols)^2 Gram matrix); the result comes back in the input's
+ *     orientation.  The norm is Frobenius, divided as ||X||_F + eps.
+ */
+#ifndef MUON_GB300_H
+#define MUON_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum muon_status {
+  MUON_OK = 0,
+  MUON_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment, dtype or scalar     */
+  MUON_ERR_UNSUPPORTED = 2,  /* no sm_103a device current, or shape out of range  */
+  MUON_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed                 */
+  MUON_ERR_TIMEOUT = 4,      /* a bounded device-side wait gave up (see status)   */
+  MUON_ERR_WORKSPACE = 5     /* workspace NULL, misaligned or too small           */
+} muon_status;
+
+typedef enum muon_dtype {
+  MUON_F32 = 0,
+  MUON_BF16 = 1
+} muon_dtype;
+
+/* One stack of same-shape 2-D weights for muon_step_grouped(). */
+typedef struct muon_group {
+  float* params;        /* [batch, rows, cols] fp32, updated in place            */
+  const void* grads;    /* [batch, rows, cols] in g_dtype, read only             */
+  float* momentum_buf;  /* [batch, rows, cols] fp32, updated in place            */
+  int g_dtype;          /* muon_dtype of grads                                   */
+  int batch;            /* 0..65535; 0 skips the group                           */
+  int rows, cols;       /* >= 1 each, <= 65536 each                              */
+  float lr_scale;       /* <= 0: max(1, rows/cols)^0.5 ([PG] 分布式细节)          */
+} muon_group;
+
+/* Kinds of kernel the library launches (trace records, launch counts). */
+typedef enum muon_kernel_kind {
+  MUON_K_PROLOGUE = 0,   /* momentum, Nesterov blend, bf16 cast, norm partials  */
+  MUON_K_SMALL_NS = 1,   /* whole step in fp32 for min(rows,cols) < 64          */
+  MUON_K_GRAM = 2,       /* A = s^2 X X^T, upper tiles + mirror                 */
+  MUON_K_POLY = 3,       /* B = b A + c A A, upper tiles + mirror               */
+  MUON_K_UPDATE = 4,     /* X <- s (a X + B X)                                  */
+  MUON_K_UPDATE_APPLY = 5/* last round: p <- (1-lr wd) p - lr scale (aX + BX)   */
+} muon_kernel_kind;
+
+/* Workspace bytes for one muon_step()/muon_ns5() call on [batch, rows, cols].
+ * Returns 0 if the sizes are invalid. */
+size_t muon_workspace_bytes(int batch, int rows, int cols);
+
+/* Workspace bytes for one muon_step_grouped() call; 0 if a group is invalid. */
+size_t muon_grouped_workspace_bytes(const muon_group* groups, int n_groups);
+
+/*
+ * zeropower_via_newtonschulz5 ([PG] 核心思想) on every matrix of a stack:
+ *   X = G / (||G||_F + eps)  (on G^T if rows > cols),
+ *   `steps` times: A = X X^T;  B = b A + c A A;  X = a X + B X,
+ *   out = X (transposed back), written as bf16 [batch, rows, cols].
+ * G: [batch, rows, cols] fp32 or bf16 (g_dtype).  steps in 1..16; batch in
+ * 0..65535, rows and cols in 1..65536 (the same limits hold for every call).
+ */
+muon_status muon_ns5(const void* G, int g_dtype, void* out_bf16,
+                     int batch, int rows, int cols, int steps,
+                     float a, float b, float c, float eps,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * One Muon step on a stack of same-shape weights ([MCS] 四, [PG] 核心思想/分布式细节):
+ *   buf <- buf + (1 - momentum) (g - buf)                 (momentum_buffer.lerp_)
+ *   u   <- g + momentum (buf - g)  if nesterov, else buf  (grad.lerp(buf, momentum))
+ *   O   <- NS(u) as in muon_ns5 (kept in fp32 for the update)
+ *   p   <- (1 - lr weight_decay) p - lr s O,   s = lr_scale > 0 ? lr_scale
+ *                                                 : max(1, rows/cols)^0.5
+ * momentum in [0, 1]; steps in 1..16; eps >= 0; all scalars finite.
+ */
+muon_status muon_step(float* params, const void* grads, int g_dtype, float* momentum_buf,
+                      int batch, int rows, int cols,
+                      float momentum, int nesterov, float lr, float weight_decay,
+                      float lr_scale, int steps, float a, float b, float c, float eps,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * muon_step on every group of a model at once (the pages stack the weights of
+ * each parameter group, [MCS] 四 第一遍/第二遍).  Groups share the scalars; the
+ * NS rounds of all tensor-core groups run as one grouped launch per stage.
+ * n_groups >= 0; groups may be NULL only when n_groups == 0.  The arrays of
+ * different groups must not overlap.
+ */
+muon_status muon_step_grouped(const muon_group* groups, int n_groups,
+                              float momentum, int nesterov, float lr, float weight_decay,
+                              int steps, float a, float b, float c, float eps,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads the workspace's sticky device error word:
+ * MUON_OK, or MUON_ERR_TIMEOUT if a bounded wait inside a kernel gave up since
+ * the word was last cleared.  clear != 0 resets the word to zero afterwards.
+ */
+muon_status muon_workspace_status(const void* workspace, size_t workspace_bytes,
+                                  void* stream, int clear);
+
+/* Static English text for a status code. */
+const char* muon_status_string(muon_status status);
+
+/* Kernels this library has launched in this process (all devices, all calls). */
+unsigned long long muon_kernel_launch_count(void);
+
+/*
+ * Optional kernel timing trace (off by default; host-side bookkeeping only).
+ * muon_trace_begin(n): from now on, record a CUDA event before and after each
+ * kernel the library launches, on that launch's stream, for up to n launches.
+ * muon_trace_end(out, max, &count): synchronise on the recorded events, fill
+ * up to `max` records (in launch order), set `count`, and stop tracing.
+ * flops/bytes are the launch's algorithmic work: for GEMM stages the dense
+ * flops of the tiles the stage is defined on (2 m^2 n for the Gram and for the
+ * update, 2 m^3 for the polynomial, each counted once for symmetric outputs
+ * as m(m+1)/2 entries), for the prologue the bytes it must move.
+ */
+typedef struct muon_trace_record {
+  int kind;        /* muon_kernel_kind                          */
+  int round;       /* NS round (0-based), -1 if not an NS stage */
+  float ms;        /* event-to-event time on the launch stream  */
+  double flops;    /* algorithmic flops of the launch           */
+  double bytes;    /* algorithmic HBM bytes of the launch       */
+} muon_trace_record;
+
+muon_status muon_trace_begin(int max_launches);
+muon_status muon_trace_end(muon_trace_record* out, int max_records, int* count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUON_GB300_H */

@@ -1,0 +1,315 @@
+"""Muon optimizer step on GB300 (sm_103a): Python binding of libmuon_gb300.so.
+
+This module only marshals arguments: it checks torch tensors (device,
+dtype, contiguity, shape), takes their device pointers and the current CUDA
+stream, and calls the C ABI declared in include/muon_gb300.h.  Every step of
+the computation runs in the library's CUDA kernels.  There is no fallback:
+if the library is not built, or no sm_103a GPU is current, calls raise.
+
+Entry points mirror the C ABI:
+  ns5(G)                         zeropower_via_newtonschulz5 on a stack of matrices
+  step(p, g, buf, ...)           one Muon step on a stack of same-shape weights
+  step_grouped([(p, g, buf)...]) one Muon step on every group of a model
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "COEFFS", "EPS", "MuonError", "load_library", "library_path", "workspace_bytes",
+    "grouped_workspace_bytes", "Workspace", "ns5", "step", "step_grouped", "GroupedStep",
+    "workspace_status", "status_string", "kernel_launch_count", "trace_begin", "trace_end",
+    "KERNEL_KINDS",
+]
+
+# Quintic coefficients and rounds as printed in "Muon Custom Sizing 实战", section 2.3.
+COEFFS = (3.4445, -4.7750, 2.0315)
+STEPS = 5
+EPS = 1e-7
+
+KERNEL_KINDS = {0: "prologue", 1: "small_ns", 2: "gram", 3: "poly", 4: "update",
+                5: "update_apply"}
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "timeout",
+           5: "workspace"}
+
+_LIB_NAME = "libmuon_gb300.so"
+_lib = None
+
+
+def library_path() -> str:
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), _LIB_NAME)
+
+
+class MuonError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+
+
+class _Group(ctypes.Structure):
+    _fields_ = [("params", ctypes.c_void_p), ("grads", ctypes.c_void_p),
+                ("momentum_buf", ctypes.c_void_p), ("g_dtype", ctypes.c_int),
+                ("batch", ctypes.c_int), ("rows", ctypes.c_int), ("cols", ctypes.c_int),
+                ("lr_scale", ctypes.c_float)]
+
+
+class _TraceRecord(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("round", ctypes.c_int), ("ms", ctypes.c_float),
+                ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
+
+
+def load_library():
+    """Load libmuon_gb300.so from this package directory (raises if it is not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is not built; run `python -m newton_schulz_step_gb300.build`")
+    L = ctypes.CDLL(path)
+    vp, ci, cf, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.muon_workspace_bytes.argtypes = [ci, ci, ci]
+    L.muon_workspace_bytes.restype = sz
+    L.muon_grouped_workspace_bytes.argtypes = [ctypes.POINTER(_Group), ci]
+    L.muon_grouped_workspace_bytes.restype = sz
+    L.muon_ns5.argtypes = [vp, ci, vp, ci, ci, ci, ci, cf, cf, cf, cf, vp, sz, vp]
+    L.muon_ns5.restype = ci
+    L.muon_step.argtypes = [vp, vp, ci, vp, ci, ci, ci, cf, ci, cf, cf, cf, ci, cf, cf, cf, cf,
+                            vp, sz, vp]
+    L.muon_step.restype = ci
+    L.muon_step_grouped.argtypes = [ctypes.POINTER(_Group), ci, cf, ci, cf, cf, ci, cf, cf, cf,
+                                    cf, vp, sz, vp]
+    L.muon_step_grouped.restype = ci
+    L.muon_workspace_status.argtypes = [vp, sz, vp, ci]
+    L.muon_workspace_status.restype = ci
+    L.muon_status_string.argtypes = [ci]
+    L.muon_status_string.restype = ctypes.c_char_p
+    L.muon_kernel_launch_count.argtypes = []
+    L.muon_kernel_launch_count.restype = ctypes.c_ulonglong
+    L.muon_trace_begin.argtypes = [ci]
+    L.muon_trace_begin.restype = ci
+    L.muon_trace_end.argtypes = [ctypes.POINTER(_TraceRecord), ci, ctypes.POINTER(ci)]
+    L.muon_trace_end.restype = ci
+    _lib = L
+    return L
+
+
+def status_string(code: int) -> str:
+    try:
+        return load_library().muon_status_string(code).decode()
+    except ImportError:
+        return _STATUS.get(code, "unknown status")
+
+
+def _raise(code: int, where: str):
+    if code != 0:
+        raise MuonError(code, where)
+
+
+def _gdt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return 0
+    if t.dtype == torch.bfloat16:
+        return 1
+    raise TypeError(f"gradients must be float32 or bfloat16, got {t.dtype}")
+
+
+def _as3d(t: torch.Tensor, name: str) -> torch.Tensor:
+    if t.dim() == 2:
+        t = t.unsqueeze(0)
+    if t.dim() != 3:
+        raise ValueError(f"{name} must be [rows, cols] or [batch, rows, cols], got {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+def workspace_bytes(batch: int, rows: int, cols: int) -> int:
+    return int(load_library().muon_workspace_bytes(batch, rows, cols))
+
+
+def _groups_array(groups):
+    arr = (_Group * max(1, len(groups)))()
+    for i, (p, g, b, s) in enumerate(groups):
+        arr[i].params = p.data_ptr() if p is not None else None
+        arr[i].grads = g.data_ptr() if g is not None else None
+        arr[i].momentum_buf = b.data_ptr() if b is not None else None
+        arr[i].g_dtype = _gdt(g) if g is not None else 1
+        arr[i].batch, arr[i].rows, arr[i].cols = (int(x) for x in g.shape)
+        arr[i].lr_scale = float(s)
+    return arr
+
+
+def grouped_workspace_bytes(shapes) -> int:
+    """shapes: iterable of (batch, rows, cols)."""
+    shapes = list(shapes)
+    arr = (_Group * max(1, len(shapes)))()
+    for i, (b, r, c) in enumerate(shapes):
+        arr[i].batch, arr[i].rows, arr[i].cols, arr[i].g_dtype = b, r, c, 1
+    return int(load_library().muon_grouped_workspace_bytes(arr, len(shapes)))
+
+
+class Workspace:
+    """Zero-filled device scratch owned by the caller (one per concurrent stream)."""
+
+    def __init__(self, nbytes: int, device=None):
+        self.tensor = torch.zeros(max(256, int(nbytes)), dtype=torch.uint8,
+                                  device=device if device is not None else "cuda")
+        if self.tensor.data_ptr() % 256:
+            raise RuntimeError("workspace allocation is not 256-byte aligned")
+
+    @property
+    def ptr(self) -> int:
+        return self.tensor.data_ptr()
+
+    @property
+    def nbytes(self) -> int:
+        return self.tensor.numel()
+
+    def ensure(self, nbytes: int):
+        if nbytes > self.nbytes:
+            self.__init__(nbytes, self.tensor.device)
+        return self
+
+
+_default_ws = {}
+
+
+def _workspace(ws, need: int, device) -> Workspace:
+    if ws is not None:
+        return ws
+    key = torch.device(device).index if torch.device(device).index is not None else \
+        torch.cuda.current_device()
+    w = _default_ws.get(key)
+    if w is None:
+        w = _default_ws[key] = Workspace(need, device)
+    return w.ensure(need)
+
+
+def ns5(G: torch.Tensor, out: torch.Tensor | None = None, steps: int = STEPS, coeffs=COEFFS,
+        eps: float = EPS, workspace: Workspace | None = None, stream=None) -> torch.Tensor:
+    """zeropower_via_newtonschulz5 of every matrix of G ([b, r, c] or [r, c]); bf16 result."""
+    L = load_library()
+    squeeze = G.dim() == 2
+    G3 = _as3d(G, "G")
+    _gdt(G3)
+    if out is None:
+        out = torch.empty(G3.shape, dtype=torch.bfloat16, device=G3.device)
+    out3 = _as3d(out, "out")
+    if out3.dtype != torch.bfloat16 or out3.shape != G3.shape:
+        raise ValueError("out must be bfloat16 with G's shape")
+    b, r, c = G3.shape
+    ws = _workspace(workspace, L.muon_workspace_bytes(b, r, c), G3.device)
+    a_, b_, c_ = coeffs
+    _raise(L.muon_ns5(G3.data_ptr(), _gdt(G3), out3.data_ptr(), b, r, c, steps, a_, b_, c_, eps,
+                      ws.ptr, ws.nbytes, _stream_handle(stream)), "muon_ns5")
+    return out3[0] if squeeze else out3
+
+
+def step(params, grads, momentum_buf, *, momentum: float, lr: float, weight_decay: float,
+         nesterov: bool = True, lr_scale: float = 0.0, steps: int = STEPS, coeffs=COEFFS,
+         eps: float = EPS, workspace: Workspace | None = None, stream=None):
+    """One Muon step, in place on params and momentum_buf (fp32, [b, r, c] or [r, c])."""
+    L = load_library()
+    p3, g3, m3 = _as3d(params, "params"), _as3d(grads, "grads"), _as3d(momentum_buf, "momentum_buf")
+    if p3.dtype != torch.float32 or m3.dtype != torch.float32:
+        raise TypeError("params and momentum_buf must be float32")
+    if not (p3.shape == g3.shape == m3.shape):
+        raise ValueError("params, grads and momentum_buf must have the same shape")
+    b, r, c = g3.shape
+    ws = _workspace(workspace, L.muon_workspace_bytes(b, r, c), g3.device)
+    a_, b_, c_ = coeffs
+    _raise(L.muon_step(p3.data_ptr(), g3.data_ptr(), _gdt(g3), m3.data_ptr(), b, r, c,
+                       momentum, int(bool(nesterov)), lr, weight_decay, lr_scale, steps,
+                       a_, b_, c_, eps, ws.ptr, ws.nbytes, _stream_handle(stream)), "muon_step")
+
+
+def _normalise_groups(groups):
+    out = []
+    for grp in groups:
+        if len(grp) == 3:
+            p, g, b = grp
+            s = 0.0
+        else:
+            p, g, b, s = grp
+        p3, g3, b3 = _as3d(p, "params"), _as3d(g, "grads"), _as3d(b, "momentum_buf")
+        if p3.dtype != torch.float32 or b3.dtype != torch.float32:
+            raise TypeError("params and momentum_buf must be float32")
+        if not (p3.shape == g3.shape == b3.shape):
+            raise ValueError("params, grads and momentum_buf must have the same shape")
+        _gdt(g3)
+        out.append((p3, g3, b3, s))
+    return out
+
+
+class GroupedStep:
+    """A prepared muon_step_grouped call: the group table is marshalled once.
+
+    Calling it enqueues one Muon step over every group on the current (or
+    given) stream.  The tensors must stay alive and in place between calls.
+    """
+
+    def __init__(self, groups, *, momentum: float, lr: float, weight_decay: float,
+                 nesterov: bool = True, steps: int = STEPS, coeffs=COEFFS, eps: float = EPS,
+                 workspace: Workspace | None = None):
+        L = load_library()
+        self._groups = _normalise_groups(groups)
+        self._arr = _groups_array(self._groups)
+        self._n = len(self._groups)
+        need = int(L.muon_grouped_workspace_bytes(self._arr, self._n))
+        if need == 0 and self._n:
+            raise ValueError("invalid group shapes")
+        dev = self._groups[0][1].device if self._n else torch.device("cuda")
+        self.workspace = workspace.ensure(need) if workspace is not None else Workspace(need, dev)
+        self._scalars = (float(momentum), int(bool(nesterov)), float(lr), float(weight_decay),
+                         int(steps), *(float(x) for x in coeffs), float(eps))
+
+    def __call__(self, stream=None):
+        L = load_library()
+        mom, nest, lr, wd, steps, a_, b_, c_, eps = self._scalars
+        _raise(L.muon_step_grouped(self._arr, self._n, mom, nest, lr, wd, steps, a_, b_, c_, eps,
+                                   self.workspace.ptr, self.workspace.nbytes,
+                                   _stream_handle(stream)), "muon_step_grouped")
+
+
+def step_grouped(groups, *, momentum: float, lr: float, weight_decay: float,
+                 nesterov: bool = True, steps: int = STEPS, coeffs=COEFFS, eps: float = EPS,
+                 workspace: Workspace | None = None, stream=None):
+    """One Muon step over every group: groups = [(params, grads, bufs[, lr_scale]), ...]."""
+    GroupedStep(groups, momentum=momentum, lr=lr, weight_decay=weight_decay, nesterov=nesterov,
+                steps=steps, coeffs=coeffs, eps=eps, workspace=workspace)(stream)
+
+
+def workspace_status(workspace: Workspace, clear: bool = False, stream=None) -> int:
+    """Synchronise and read the workspace's sticky device error word (0 = ok, 4 = timeout)."""
+    return int(load_library().muon_workspace_status(workspace.ptr, workspace.nbytes,
+                                                    _stream_handle(stream), int(clear)))
+
+
+def kernel_launch_count() -> int:
+    return int(load_library().muon_kernel_launch_count())
+
+
+def trace_begin(max_launches: int = 4096):
+    _raise(load_library().muon_trace_begin(max_launches), "muon_trace_begin")
+
+
+def trace_end(max_records: int = 4096):
+    """Stop tracing; list of {kind, round, ms, flops, bytes} in launch order."""
+    recs = (_TraceRecord * max(1, max_records))()
+    n = ctypes.c_int(0)
+    _raise(load_library().muon_trace_end(recs, max_records, ctypes.byref(n)), "muon_trace_end")
+    return [{"kind": KERNEL_KINDS.get(r.kind, str(r.kind)), "round": r.round, "ms": r.ms,
+             "flops": r.flops, "bytes": r.bytes} for r in recs[: n.value]]

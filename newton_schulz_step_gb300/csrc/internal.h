@@ -1,0 +1,110 @@
+// internal.h -- argument blocks shared by the host planner and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/muon_gb300.h"
+
+namespace muon {
+
+constexpr int kTileM = 128;       // GEMM tile rows (UMMA M)
+constexpr int kTileK = 64;        // bf16 elements per 128-byte swizzle row
+constexpr int kSmallMaxM = 63;    // min(rows, cols) below 64 takes the fp32 path
+constexpr int kMaxParts = 32;     // norm partial sums per matrix
+constexpr int kMaxProblems = 8;   // groups per grouped GEMM launch
+constexpr int kMaxSmallGroups = 16;
+
+// Bits of the sticky device error word (first word of the workspace).
+enum DeviceError : unsigned int {
+  kErrTimeoutProducer = 1u,
+  kErrTimeoutMma = 2u,
+  kErrTimeoutEpilogue = 4u,
+  kErrTimeoutDrain = 8u,
+};
+
+// What the prologue computes from (g, buf).
+enum PrologueMode : int {
+  kPrologueNsOnly = 0,       // u = g (muon_ns5)
+  kPrologueNesterov = 1,     // buf <- lerp(buf, g, 1-beta); u = lerp(g, buf, beta)
+  kProloguePlain = 2,        // buf <- lerp(buf, g, 1-beta); u = buf
+};
+
+struct PrologueArgs {
+  const void* g;          // [batch, r, c] fp32 or bf16
+  float* buf;             // [batch, r, c] fp32 (unused in kPrologueNsOnly)
+  __nv_bfloat16* x;       // [batch, m, ldx] bf16: u, or u^T when r > c
+  float* parts;           // [batch, nparts] partial sums of u^2
+  int batch, r, c, ldx;
+  int nparts;             // blocks per matrix (<= kMaxParts)
+  float beta;
+};
+
+// One group of the fp32 small-matrix path.
+struct SmallGroup {
+  const void* g;
+  float* buf;
+  float* param;           // step mode
+  __nv_bfloat16* out;     // ns5 mode
+  float* x;               // workspace [batch, m, n] fp32
+  int gdt;                // muon_dtype
+  int batch, r, c;
+  int block_begin;        // first block index of this group in the launch
+  float lr_eff;           // lr * rescale
+};
+
+struct SmallLaunch {
+  SmallGroup grp[kMaxSmallGroups];
+  int n_groups;
+  int mode;               // PrologueMode
+  int steps;
+  float beta, a, b, c, eps, decay;
+};
+
+// Output of the last update round.
+enum OutMode : int { kOutX = 0, kOutParam = 1, kOutBf16 = 2 };
+
+struct GemmProblem {
+  int batch, m, n;        // X is m x n (m <= n), batch matrices
+  int ldx, lda;           // padded leading dimensions (elements) of X and A/B
+  int tiles_m, tiles_n;   // tile grid of this stage's output
+  int tiles_per_mat;
+  int tile_begin;         // first linear tile index of this problem
+  int k_blocks;           // ceil(K / kTileK)
+  const __nv_bfloat16* x_cur;   // update: X of this round (a X term)
+  __nv_bfloat16* x_next;        // update: next X (kOutX)
+  const __nv_bfloat16* a_mat;   // poly: A (b A term)
+  __nv_bfloat16* sym_out;       // gram: A, poly: B
+  const float* parts;           // norm partials [batch, nparts]
+  int nparts;
+  int first_round;              // fold s = 1/(||u||_F + eps) in
+  int out_mode;                 // OutMode
+  int tall;                     // original rows > cols: outputs are transposed back
+  float* param;                 // kOutParam: [batch, rows, cols] fp32
+  __nv_bfloat16* out;           // kOutBf16: [batch, rows, cols]
+  float lr_eff, decay;
+};
+
+struct GemmLaunch {
+  CUtensorMap tm_a[kMaxProblems];   // operand A tiles (box 64 x 128)
+  CUtensorMap tm_b[kMaxProblems];   // operand B tiles
+  GemmProblem prob[kMaxProblems];
+  int n_prob;
+  int total_tiles;
+  float a, b, c, eps;
+  unsigned int* status;             // sticky device error word
+};
+
+enum GemmStage : int { kStageGram = 0, kStagePoly = 1, kStageUpdate = 2 };
+
+// Launchers (defined next to their kernels).  Each returns a cudaError_t from
+// the launch; grid sizes come from the caller's SM count.
+cudaError_t launch_prologue(const PrologueArgs& a, int mode, int gdt, cudaStream_t s);
+cudaError_t launch_small(const SmallLaunch& l, int total_blocks, cudaStream_t s);
+cudaError_t launch_gemm(const GemmLaunch& l, int stage, int bn, int grid, cudaStream_t s);
+int gemm_smem_bytes(int stage, int bn);
+
+}  // namespace muon

@@ -1,0 +1,634 @@
+// muon_api.cu -- host side of the C ABI declared in include/muon_gb300.h:
+// argument validation, workspace planning, TMA tensor maps, and the launch
+// sequence of one Muon step:
+//
+//   small groups (min(rows,cols) < 64):  one fp32 kernel, whole step
+//   tensor-core groups:                  prologue per group, then per NS round
+//                                        Gram -> Poly -> Update, each one
+//                                        grouped persistent launch over all
+//                                        groups (up to kMaxProblems at a time)
+//
+// Everything is enqueued on the caller's stream; nothing here synchronises
+// (except muon_workspace_status and muon_trace_end) or allocates device memory.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+
+using namespace muon;
+
+namespace {
+
+// ------------------------------------------------------------ bookkeeping
+std::atomic<unsigned long long> g_launch_count{0};
+
+struct TraceSlot {
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  int kind = 0, round = -1;
+  double flops = 0, bytes = 0;
+};
+
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+int g_trace_cap = 0;
+std::vector<TraceSlot> g_trace;
+
+struct LaunchInfo {
+  int kind;
+  int round;
+  double flops;
+  double bytes;
+};
+
+// Runs `fn` (which launches one kernel), counting it and, when tracing,
+// bracketing it with events on `st`.
+template <typename F>
+cudaError_t tracked_launch(cudaStream_t st, const LaunchInfo& info, F&& fn) {
+  TraceSlot* slot = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (g_trace_on && static_cast<int>(g_trace.size()) < g_trace_cap) {
+      TraceSlot ts;
+      ts.kind = info.kind;
+      ts.round = info.round;
+      ts.flops = info.flops;
+      ts.bytes = info.bytes;
+      if (cudaEventCreate(&ts.e0) == cudaSuccess && cudaEventCreate(&ts.e1) == cudaSuccess) {
+        g_trace.push_back(ts);
+        slot = &g_trace.back();
+        cudaEventRecord(slot->e0, st);
+      }
+    }
+  }
+  const cudaError_t e = fn();
+  g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  if (slot) cudaEventRecord(slot->e1, st);
+  return e;
+}
+
+// ------------------------------------------------------------ device info
+struct DevInfo {
+  int checked = 0;
+  int ok = 0;
+  int sms = 0;
+};
+DevInfo g_dev[64];
+std::mutex g_dev_mu;
+
+muon_status current_device(int* sms) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return MUON_ERR_UNSUPPORTED;
+  if (dev >= 64) return MUON_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.checked) {
+    int maj = 0, min = 0, n = 0;
+    if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MUON_ERR_CUDA;
+    d.checked = 1;
+    d.ok = (maj == 10 && min == 3);  // the cubin is built for sm_103a only
+    d.sms = n;
+  }
+  if (!d.ok) return MUON_ERR_UNSUPPORTED;
+  *sms = d.sms;
+  return MUON_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// bf16 [batch][rows][ld] with logical width `cols`; box = 64 columns x box_rows,
+// 128-byte swizzle, out-of-bounds elements read as zero.
+bool make_tmap(CUtensorMap* tm, const void* base, int cols, int rows, int batch, int ld,
+               int box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2,
+                                 static_cast<cuuint64_t>(ld) * 2 * static_cast<cuuint64_t>(rows)};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ planning
+struct GPlan {
+  // caller arrays
+  float* p = nullptr;
+  const void* g = nullptr;
+  float* buf = nullptr;
+  __nv_bfloat16* out = nullptr;
+  int gdt = 0;
+  int batch = 0, r = 0, c = 0;
+  float lr_scale = 0.f;
+  // derived
+  int m = 0, n = 0;
+  bool tall = false, small = false;
+  int ldx = 0, lda = 0, nparts = 0;
+  size_t x0 = 0, x1 = 0, am = 0, bm = 0, parts = 0, xs = 0;  // workspace offsets
+};
+
+constexpr size_t kStatusBytes = 256;
+constexpr int kMaxDim = 65536;
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+int round_up(int x, int a) { return (x + a - 1) / a * a; }
+int cdiv(int x, int a) { return (x + a - 1) / a; }
+
+bool shape_ok(int batch, int r, int c) {
+  return batch >= 0 && batch <= 65535 && r >= 1 && c >= 1 && r <= kMaxDim && c <= kMaxDim;
+}
+
+// Fills the derived fields and workspace offsets; returns the total bytes.
+size_t plan_workspace(std::vector<GPlan>& gs) {
+  size_t off = kStatusBytes;
+  for (GPlan& g : gs) {
+    g.tall = g.r > g.c;
+    g.m = std::min(g.r, g.c);
+    g.n = std::max(g.r, g.c);
+    g.small = g.m <= kSmallMaxM;
+    if (g.batch == 0) continue;
+    const size_t b = static_cast<size_t>(g.batch);
+    if (g.small) {
+      g.xs = off;
+      off += align256(b * g.m * g.n * sizeof(float));
+    } else {
+      g.ldx = round_up(g.n, 8);
+      g.lda = round_up(g.m, 8);
+      const size_t xb = align256(b * g.m * static_cast<size_t>(g.ldx) * 2);
+      const size_t ab = align256(b * g.m * static_cast<size_t>(g.lda) * 2);
+      g.x0 = off; off += xb;
+      g.x1 = off; off += xb;
+      g.am = off; off += ab;
+      g.bm = off; off += ab;
+      const int tiles = cdiv(g.r, 64) * cdiv(g.c, 64);
+      g.nparts = std::min(tiles, kMaxParts);
+      g.parts = off;
+      off += align256(b * g.nparts * sizeof(float));
+    }
+  }
+  return off;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool finite(float x) { return std::isfinite(x); }
+
+struct Scalars {
+  int mode;  // PrologueMode
+  float beta, lr, wd;
+  int steps;
+  float a, b, c, eps;
+};
+
+muon_status check_scalars(const Scalars& s) {
+  if (s.steps < 1 || s.steps > 16) return MUON_ERR_INVALID_ARG;
+  if (!finite(s.a) || !finite(s.b) || !finite(s.c) || !finite(s.eps) || s.eps < 0.f)
+    return MUON_ERR_INVALID_ARG;
+  if (s.mode != kPrologueNsOnly) {
+    if (!finite(s.beta) || s.beta < 0.f || s.beta > 1.f) return MUON_ERR_INVALID_ARG;
+    if (!finite(s.lr) || !finite(s.wd)) return MUON_ERR_INVALID_ARG;
+  }
+  return MUON_OK;
+}
+
+muon_status check_group(const GPlan& g, int mode) {
+  if (!shape_ok(g.batch, g.r, g.c)) return MUON_ERR_INVALID_ARG;
+  if (g.gdt != MUON_F32 && g.gdt != MUON_BF16) return MUON_ERR_INVALID_ARG;
+  if (!finite(g.lr_scale)) return MUON_ERR_INVALID_ARG;
+  if (g.batch == 0) return MUON_OK;
+  if (!g.g || !aligned16(g.g)) return MUON_ERR_INVALID_ARG;
+  if (mode == kPrologueNsOnly) {
+    if (!g.out || !aligned16(g.out)) return MUON_ERR_INVALID_ARG;
+  } else {
+    if (!g.p || !g.buf || !aligned16(g.p) || !aligned16(g.buf)) return MUON_ERR_INVALID_ARG;
+  }
+  return MUON_OK;
+}
+
+// ------------------------------------------------------------ GEMM launch setup
+struct StageShape {
+  int tiles_m, tiles_n, tiles_per_mat, k_blocks;
+};
+
+StageShape stage_shape(const GPlan& g, int stage, int bn) {
+  StageShape s{};
+  if (stage == kStageUpdate) {
+    s.tiles_m = cdiv(g.m, kTileM);
+    s.tiles_n = cdiv(g.n, bn);
+    s.tiles_per_mat = s.tiles_m * s.tiles_n;
+    s.k_blocks = cdiv(g.m, kTileK);
+  } else {
+    s.tiles_m = cdiv(g.m, kTileM);
+    s.tiles_n = cdiv(g.m, bn);
+    s.tiles_per_mat = 0;
+    for (int tm = 0; tm < s.tiles_m; ++tm) s.tiles_per_mat += s.tiles_n - (tm * kTileM) / bn;
+    s.k_blocks = cdiv(stage == kStageGram ? g.n : g.m, kTileK);
+  }
+  return s;
+}
+
+double stage_flops(const GPlan& g, int stage) {
+  const double m = g.m, n = g.n, b = g.batch;
+  if (stage == kStageGram) return b * n * m * (m + 1);      // m(m+1)/2 entries x 2n
+  if (stage == kStagePoly) return b * m * m * (m + 1);      // m(m+1)/2 entries x 2m
+  return b * 2.0 * m * m * n;
+}
+
+// Builds the launch block of one stage for a chunk of tensor-core groups.
+// `cur` selects X0 (0) or X1 (1) as this round's X.
+muon_status build_gemm(GemmLaunch& L, const std::vector<GPlan*>& chunk, int stage, int bn,
+                       int cur, bool first_round, bool last_round, int mode, const Scalars& sc,
+                       uint8_t* ws) {
+  std::memset(&L, 0, sizeof(L));
+  // heaviest problems first: their tiles are handed out first
+  std::vector<GPlan*> order(chunk);
+  std::stable_sort(order.begin(), order.end(), [&](GPlan* x, GPlan* y) {
+    const StageShape sx = stage_shape(*x, stage, bn), sy = stage_shape(*y, stage, bn);
+    return sx.k_blocks > sy.k_blocks;
+  });
+  int tiles = 0;
+  for (size_t i = 0; i < order.size(); ++i) {
+    const GPlan& g = *order[i];
+    GemmProblem& P = L.prob[i];
+    const StageShape ss = stage_shape(g, stage, bn);
+    P.batch = g.batch;
+    P.m = g.m;
+    P.n = g.n;
+    P.ldx = g.ldx;
+    P.lda = g.lda;
+    P.tiles_m = ss.tiles_m;
+    P.tiles_n = ss.tiles_n;
+    P.tiles_per_mat = ss.tiles_per_mat;
+    P.k_blocks = ss.k_blocks;
+    P.tile_begin = tiles;
+    tiles += ss.tiles_per_mat * g.batch;
+    const uint8_t* xc = ws + (cur ? g.x1 : g.x0);
+    uint8_t* xn = ws + (cur ? g.x0 : g.x1);
+    P.x_cur = reinterpret_cast<const __nv_bfloat16*>(xc);
+    P.x_next = reinterpret_cast<__nv_bfloat16*>(xn);
+    P.a_mat = reinterpret_cast<const __nv_bfloat16*>(ws + g.am);
+    P.sym_out = reinterpret_cast<__nv_bfloat16*>(ws + (stage == kStageGram ? g.am : g.bm));
+    P.parts = reinterpret_cast<const float*>(ws + g.parts);
+    P.nparts = g.nparts;
+    P.first_round = first_round ? 1 : 0;
+    P.out_mode = !last_round ? kOutX : (mode == kPrologueNsOnly ? kOutBf16 : kOutParam);
+    P.tall = g.tall ? 1 : 0;
+    P.param = g.p;
+    P.out = g.out;
+    const float scale = g.lr_scale > 0.f ? g.lr_scale
+                                          : static_cast<float>(std::sqrt(std::max(
+                                                1.0, static_cast<double>(g.r) / g.c)));
+    P.lr_eff = sc.lr * scale;
+    P.decay = 1.0f - sc.lr * sc.wd;
+    bool ok = true;
+    if (stage == kStageGram) {
+      ok = make_tmap(&L.tm_a[i], xc, g.n, g.m, g.batch, g.ldx, kTileM) &&
+           make_tmap(&L.tm_b[i], xc, g.n, g.m, g.batch, g.ldx, bn);
+    } else if (stage == kStagePoly) {
+      ok = make_tmap(&L.tm_a[i], ws + g.am, g.m, g.m, g.batch, g.lda, kTileM) &&
+           make_tmap(&L.tm_b[i], ws + g.am, g.m, g.m, g.batch, g.lda, bn);
+    } else {
+      ok = make_tmap(&L.tm_a[i], ws + g.bm, g.m, g.m, g.batch, g.lda, kTileM) &&
+           make_tmap(&L.tm_b[i], xc, g.n, g.m, g.batch, g.ldx, 64);
+    }
+    if (!ok) return MUON_ERR_CUDA;
+  }
+  L.n_prob = static_cast<int>(order.size());
+  L.total_tiles = tiles;
+  L.a = sc.a;
+  L.b = sc.b;
+  L.c = sc.c;
+  L.eps = sc.eps;
+  L.status = reinterpret_cast<unsigned int*>(ws);
+  return MUON_OK;
+}
+
+// ------------------------------------------------------------ the step
+muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
+                     size_t ws_bytes, cudaStream_t st) {
+  muon_status s = check_scalars(sc);
+  if (s != MUON_OK) return s;
+  for (const GPlan& g : gs) {
+    s = check_group(g, sc.mode);
+    if (s != MUON_OK) return s;
+  }
+  const size_t need = plan_workspace(gs);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || ws_bytes < need)
+    return MUON_ERR_WORKSPACE;
+  bool any = false;
+  for (const GPlan& g : gs) any |= g.batch > 0;
+  if (!any) return MUON_OK;
+
+  int sms = 0;
+  s = current_device(&sms);
+  if (s != MUON_OK) return s;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+
+  // -- small matrices: one fp32 kernel for all of them
+  {
+    SmallLaunch sl;
+    std::memset(&sl, 0, sizeof(sl));
+    sl.mode = sc.mode;
+    sl.steps = sc.steps;
+    sl.beta = sc.beta;
+    sl.a = sc.a;
+    sl.b = sc.b;
+    sl.c = sc.c;
+    sl.eps = sc.eps;
+    sl.decay = 1.0f - sc.lr * sc.wd;
+    int blocks = 0;
+    auto flush = [&]() -> muon_status {
+      if (sl.n_groups == 0) return MUON_OK;
+      double bytes = 0;
+      for (int i = 0; i < sl.n_groups; ++i)
+        bytes += static_cast<double>(sl.grp[i].batch) * sl.grp[i].r * sl.grp[i].c *
+                 (sc.mode == kPrologueNsOnly ? 6.0 : 20.0);
+      const cudaError_t e = tracked_launch(st, {MUON_K_SMALL_NS, -1, 0.0, bytes},
+                                           [&] { return launch_small(sl, blocks, st); });
+      sl.n_groups = 0;
+      blocks = 0;
+      return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+    };
+    for (GPlan& g : gs) {
+      if (!g.small || g.batch == 0) continue;
+      SmallGroup& sg = sl.grp[sl.n_groups++];
+      sg.g = g.g;
+      sg.buf = g.buf;
+      sg.param = g.p;
+      sg.out = g.out;
+      sg.x = reinterpret_cast<float*>(ws + g.xs);
+      sg.gdt = g.gdt;
+      sg.batch = g.batch;
+      sg.r = g.r;
+      sg.c = g.c;
+      sg.block_begin = blocks;
+      const float scale = g.lr_scale > 0.f ? g.lr_scale
+                                            : static_cast<float>(std::sqrt(std::max(
+                                                  1.0, static_cast<double>(g.r) / g.c)));
+      sg.lr_eff = sc.lr * scale;
+      blocks += g.batch;
+      if (sl.n_groups == kMaxSmallGroups) {
+        s = flush();
+        if (s != MUON_OK) return s;
+      }
+    }
+    s = flush();
+    if (s != MUON_OK) return s;
+  }
+
+  // -- tensor-core matrices
+  std::vector<GPlan*> big;
+  for (GPlan& g : gs)
+    if (!g.small && g.batch > 0) big.push_back(&g);
+  for (GPlan* gp : big) {
+    const GPlan& g = *gp;
+    PrologueArgs pa;
+    pa.g = g.g;
+    pa.buf = g.buf;
+    pa.x = reinterpret_cast<__nv_bfloat16*>(ws + g.x0);
+    pa.parts = reinterpret_cast<float*>(ws + g.parts);
+    pa.batch = g.batch;
+    pa.r = g.r;
+    pa.c = g.c;
+    pa.ldx = g.ldx;
+    pa.nparts = g.nparts;
+    pa.beta = sc.beta;
+    const double elems = static_cast<double>(g.batch) * g.r * g.c;
+    const double bytes = elems * ((g.gdt == MUON_BF16 ? 2.0 : 4.0) + 2.0 +
+                                  (sc.mode == kPrologueNsOnly ? 0.0 : 8.0));
+    const cudaError_t e = tracked_launch(st, {MUON_K_PROLOGUE, -1, 0.0, bytes},
+                                         [&] { return launch_prologue(pa, sc.mode, g.gdt, st); });
+    if (e != cudaSuccess) return MUON_ERR_CUDA;
+  }
+
+  for (size_t c0 = 0; c0 < big.size(); c0 += kMaxProblems) {
+    std::vector<GPlan*> chunk(big.begin() + c0,
+                              big.begin() + std::min(big.size(), c0 + kMaxProblems));
+    int max_n = 0;
+    for (GPlan* g : chunk) max_n = std::max(max_n, g->n);
+    const int bn_upd = max_n > 128 ? 256 : 128;
+    for (int it = 0; it < sc.steps; ++it) {
+      const int cur = it & 1;
+      const bool first = (it == 0), last = (it == sc.steps - 1);
+      const int stages[3] = {kStageGram, kStagePoly, kStageUpdate};
+      for (int stage : stages) {
+        const int bn = (stage == kStageUpdate) ? bn_upd : 128;
+        GemmLaunch L;
+        s = build_gemm(L, chunk, stage, bn, cur, first, last, sc.mode, sc, ws);
+        if (s != MUON_OK) return s;
+        if (L.total_tiles == 0) continue;
+        double flops = 0, bytes = 0;
+        for (GPlan* g : chunk) {
+          flops += stage_flops(*g, stage);
+          if (stage == kStageUpdate && last && sc.mode != kPrologueNsOnly)
+            bytes += static_cast<double>(g->batch) * g->m * g->n * 8.0;
+        }
+        const int kind = stage == kStageGram   ? MUON_K_GRAM
+                         : stage == kStagePoly ? MUON_K_POLY
+                         : last                ? MUON_K_UPDATE_APPLY
+                                               : MUON_K_UPDATE;
+        const int grid = std::min(L.total_tiles, sms);
+        const cudaError_t e = tracked_launch(st, {kind, it, flops, bytes},
+                                             [&] { return launch_gemm(L, stage, bn, grid, st); });
+        if (e != cudaSuccess) return MUON_ERR_CUDA;
+      }
+    }
+  }
+  return MUON_OK;
+}
+
+GPlan make_plan(float* p, const void* g, int gdt, float* buf, __nv_bfloat16* out, int batch,
+                int r, int c, float lr_scale) {
+  GPlan x;
+  x.p = p;
+  x.g = g;
+  x.gdt = gdt;
+  x.buf = buf;
+  x.out = out;
+  x.batch = batch;
+  x.r = r;
+  x.c = c;
+  x.lr_scale = lr_scale;
+  return x;
+}
+
+}  // namespace
+
+// ============================================================ C ABI
+extern "C" {
+
+size_t muon_workspace_bytes(int batch, int rows, int cols) {
+  if (!shape_ok(batch, rows, cols)) return 0;
+  std::vector<GPlan> gs{make_plan(nullptr, nullptr, MUON_BF16, nullptr, nullptr, batch, rows,
+                                  cols, 0.f)};
+  return plan_workspace(gs);
+}
+
+size_t muon_grouped_workspace_bytes(const muon_group* groups, int n_groups) {
+  if (n_groups < 0 || (n_groups > 0 && !groups)) return 0;
+  std::vector<GPlan> gs;
+  for (int i = 0; i < n_groups; ++i) {
+    const muon_group& g = groups[i];
+    if (!shape_ok(g.batch, g.rows, g.cols)) return 0;
+    gs.push_back(make_plan(nullptr, nullptr, g.g_dtype, nullptr, nullptr, g.batch, g.rows,
+                           g.cols, g.lr_scale));
+  }
+  return plan_workspace(gs);
+}
+
+muon_status muon_ns5(const void* G, int g_dtype, void* out_bf16, int batch, int rows, int cols,
+                     int steps, float a, float b, float c, float eps, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  try {
+    std::vector<GPlan> gs{make_plan(nullptr, G, g_dtype, nullptr,
+                                    static_cast<__nv_bfloat16*>(out_bf16), batch, rows, cols,
+                                    0.f)};
+    const Scalars sc{kPrologueNsOnly, 0.f, 0.f, 0.f, steps, a, b, c, eps};
+    return run_step(gs, sc, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+  } catch (...) {
+    return MUON_ERR_CUDA;
+  }
+}
+
+muon_status muon_step(float* params, const void* grads, int g_dtype, float* momentum_buf,
+                      int batch, int rows, int cols, float momentum, int nesterov, float lr,
+                      float weight_decay, float lr_scale, int steps, float a, float b, float c,
+                      float eps, void* workspace, size_t workspace_bytes, void* stream) {
+  try {
+    std::vector<GPlan> gs{make_plan(params, grads, g_dtype, momentum_buf, nullptr, batch, rows,
+                                    cols, lr_scale)};
+    const Scalars sc{nesterov ? kPrologueNesterov : kProloguePlain, momentum, lr, weight_decay,
+                     steps, a, b, c, eps};
+    return run_step(gs, sc, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+  } catch (...) {
+    return MUON_ERR_CUDA;
+  }
+}
+
+muon_status muon_step_grouped(const muon_group* groups, int n_groups, float momentum,
+                              int nesterov, float lr, float weight_decay, int steps, float a,
+                              float b, float c, float eps, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  try {
+    if (n_groups < 0 || (n_groups > 0 && !groups)) return MUON_ERR_INVALID_ARG;
+    std::vector<GPlan> gs;
+    gs.reserve(n_groups);
+    for (int i = 0; i < n_groups; ++i) {
+      const muon_group& g = groups[i];
+      gs.push_back(make_plan(g.params, g.grads, g.g_dtype, g.momentum_buf, nullptr, g.batch,
+                             g.rows, g.cols, g.lr_scale));
+    }
+    const Scalars sc{nesterov ? kPrologueNesterov : kProloguePlain, momentum, lr, weight_decay,
+                     steps, a, b, c, eps};
+    return run_step(gs, sc, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+  } catch (...) {
+    return MUON_ERR_CUDA;
+  }
+}
+
+muon_status muon_workspace_status(const void* workspace, size_t workspace_bytes, void* stream,
+                                  int clear) {
+  if (!workspace || workspace_bytes < kStatusBytes ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MUON_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned int word = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MUON_ERR_CUDA;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MUON_ERR_CUDA;
+  if (clear && cudaMemsetAsync(const_cast<void*>(workspace), 0, sizeof(word), st) != cudaSuccess)
+    return MUON_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MUON_ERR_CUDA;
+  return word ? MUON_ERR_TIMEOUT : MUON_OK;
+}
+
+const char* muon_status_string(muon_status status) {
+  switch (status) {
+    case MUON_OK:
+      return "ok";
+    case MUON_ERR_INVALID_ARG:
+      return "invalid argument";
+    case MUON_ERR_UNSUPPORTED:
+      return "unsupported device or shape (needs an sm_103a GPU)";
+    case MUON_ERR_CUDA:
+      return "CUDA error";
+    case MUON_ERR_TIMEOUT:
+      return "a bounded device-side wait timed out";
+    case MUON_ERR_WORKSPACE:
+      return "workspace missing, misaligned or too small";
+  }
+  return "unknown status";
+}
+
+unsigned long long muon_kernel_launch_count(void) {
+  return g_launch_count.load(std::memory_order_relaxed);
+}
+
+muon_status muon_trace_begin(int max_launches) {
+  if (max_launches < 0) return MUON_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  for (TraceSlot& t : g_trace) {
+    if (t.e0) cudaEventDestroy(t.e0);
+    if (t.e1) cudaEventDestroy(t.e1);
+  }
+  g_trace.clear();
+  g_trace.reserve(max_launches);
+  g_trace_cap = max_launches;
+  g_trace_on = true;
+  return MUON_OK;
+}
+
+muon_status muon_trace_end(muon_trace_record* out, int max_records, int* count) {
+  if (max_records < 0 || (max_records > 0 && !out)) return MUON_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_on = false;
+  muon_status st = MUON_OK;
+  int n = 0;
+  for (TraceSlot& t : g_trace) {
+    if (n < max_records) {
+      float ms = 0.f;
+      if (cudaEventSynchronize(t.e1) != cudaSuccess ||
+          cudaEventElapsedTime(&ms, t.e0, t.e1) != cudaSuccess)
+        st = MUON_ERR_CUDA;
+      out[n].kind = t.kind;
+      out[n].round = t.round;
+      out[n].ms = ms;
+      out[n].flops = t.flops;
+      out[n].bytes = t.bytes;
+      ++n;
+    }
+    cudaEventDestroy(t.e0);
+    cudaEventDestroy(t.e1);
+  }
+  g_trace.clear();
+  if (count) *count = n;
+  return st;
+}
+
+}  // extern "C"

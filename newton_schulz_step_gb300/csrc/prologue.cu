@@ -1,0 +1,222 @@
+// prologue.cu -- the elementwise head of the Muon step, one pass over HBM:
+//
+//   buf <- buf + (1 - beta) (g - buf)        momentum_buffer.lerp_(grad, 1 - momentum)
+//   u   <- g + beta (buf - g)                grad.lerp(momentum_buffer, momentum)
+//                                            (or u = buf without Nesterov, u = g for NS only)
+//   X   <- bf16(u), or bf16(u^T) when rows > cols (padded leading dimension)
+//   partial sums of u^2 for the Frobenius norm, one per block
+//
+// ("Muon Custom Sizing 实战", section 四, second pass; the norm is the X.norm()
+// of "parameter-golf train_gpt.py 源码精读", section 核心思想.)  The division by
+// ||u||_F + eps is folded into the first Gram and update epilogues, which sum
+// the partials in a fixed order, so the result is deterministic.
+//
+// Grid: (nparts, batch); block b of matrix z walks the 64x64 tiles
+// b, b + nparts, ... of that matrix.  Each thread moves 2 x 8 consecutive
+// elements of a tile row with 16-byte accesses; rows > cols tiles are
+// transposed through shared memory so the X stores stay coalesced.
+#include "internal.h"
+
+namespace muon {
+
+namespace {
+
+template <int GDT>
+__device__ __forceinline__ void load_g8(const void* g, size_t idx, bool vec, int valid,
+                                        float (&out)[8]) {
+  if (GDT == MUON_BF16) {
+    const __nv_bfloat16* gp = static_cast<const __nv_bfloat16*>(g) + idx;
+    if (vec) {
+      const uint4 w = *reinterpret_cast<const uint4*>(gp);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[h]));
+        out[2 * h] = f.x;
+        out[2 * h + 1] = f.y;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) out[e] = (e < valid) ? __bfloat162float(gp[e]) : 0.f;
+    }
+  } else {
+    const float* gp = static_cast<const float*>(g) + idx;
+    if (vec) {
+      const float4 a = *reinterpret_cast<const float4*>(gp);
+      const float4 b = *reinterpret_cast<const float4*>(gp + 4);
+      out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+      out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) out[e] = (e < valid) ? gp[e] : 0.f;
+    }
+  }
+}
+
+__device__ __forceinline__ void load_f8(const float* p, bool vec, int valid, float (&out)[8]) {
+  if (vec) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+    out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+    out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) out[e] = (e < valid) ? p[e] : 0.f;
+  }
+}
+
+__device__ __forceinline__ void store_f8(float* p, bool vec, int valid, const float (&v)[8]) {
+  if (vec) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (e < valid) p[e] = v[e];
+  }
+}
+
+__device__ __forceinline__ void store_bf8(__nv_bfloat16* p, bool vec, int valid,
+                                          const float (&v)[8]) {
+  if (vec) {
+    uint32_t ws[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * h], v[2 * h + 1]);
+      ws[h] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (e < valid) p[e] = __float2bfloat16_rn(v[e]);
+  }
+}
+
+template <int MODE, int GDT, bool TALL>
+__global__ void __launch_bounds__(256) prologue_kernel(const PrologueArgs A) {
+  __shared__ float stage_tile[TALL ? 64 : 1][65];
+  __shared__ float red[8];
+  const int mat = blockIdx.y;
+  const int part = blockIdx.x;
+  const int r = A.r, c = A.c;
+  const int tiles_c = (c + 63) / 64;
+  const int ntiles = ((r + 63) / 64) * tiles_c;
+  const size_t moff = static_cast<size_t>(mat) * r * c;
+  const int m = TALL ? c : r;
+  __nv_bfloat16* xm = A.x + static_cast<size_t>(mat) * m * A.ldx;
+  const int tid = threadIdx.x;
+  const int ty = tid >> 3;        // tile row within a 32-row half
+  const int tx = (tid & 7) * 8;   // first of 8 tile columns
+  const bool cvec = (c & 7) == 0; // rows start 16-byte aligned
+  const float beta = A.beta;
+  float sumsq = 0.f;
+
+  for (int tile = part; tile < ntiles; tile += A.nparts) {
+    const int tr = tile / tiles_c;
+    const int tc = tile - tr * tiles_c;
+    const int cc = tc * 64 + tx;
+    const int valid = max(0, min(8, c - cc));
+    float gv[2][8], bv[2][8];
+    // all loads of the tile first, so both halves are in flight together
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int rr = tr * 64 + ty + 32 * h;
+      const bool in = rr < r && valid > 0;
+      const size_t idx = moff + static_cast<size_t>(rr) * c + cc;
+      if (in) {
+        load_g8<GDT>(A.g, idx, cvec && valid == 8, valid, gv[h]);
+        if (MODE != kPrologueNsOnly) load_f8(A.buf + idx, cvec && valid == 8, valid, bv[h]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) gv[h][e] = bv[h][e] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int rr = tr * 64 + ty + 32 * h;
+      const bool in = rr < r && valid > 0;
+      const size_t idx = moff + static_cast<size_t>(rr) * c + cc;
+      float u[8];
+      if (MODE == kPrologueNsOnly) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) u[e] = gv[h][e];
+      } else {
+        float nb[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          nb[e] = fmaf(1.0f - beta, gv[h][e] - bv[h][e], bv[h][e]);
+          u[e] = (MODE == kPrologueNesterov) ? fmaf(beta, nb[e] - gv[h][e], gv[h][e]) : nb[e];
+        }
+        if (in) store_f8(A.buf + idx, cvec && valid == 8, valid, nb);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sumsq = fmaf(u[e], u[e], sumsq);
+      if (!TALL) {
+        if (in) store_bf8(xm + static_cast<size_t>(rr) * A.ldx + cc, valid == 8, valid, u);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) stage_tile[ty + 32 * h][tx + e] = u[e];
+      }
+    }
+    if (TALL) {
+      // X = u^T: X row (original column) tc*64 + ..., X columns tr*64 + ...
+      __syncthreads();
+      const int xc = tr * 64 + tx;                 // X column = original row
+      const int xvalid = max(0, min(8, r - xc));
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int xr = tc * 64 + ty + 32 * h;      // X row = original column
+        if (xr < c && xvalid > 0) {
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = stage_tile[tx + e][ty + 32 * h];
+          store_bf8(xm + static_cast<size_t>(xr) * A.ldx + xc, xvalid == 8, xvalid, v);
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // deterministic block reduction of sum(u^2)
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sumsq += __shfl_xor_sync(0xffffffffu, sumsq, o);
+  if ((tid & 31) == 0) red[tid >> 5] = sumsq;
+  __syncthreads();
+  if (tid == 0) {
+    float t = 0.f;
+    for (int w = 0; w < 8; ++w) t += red[w];
+    A.parts[static_cast<size_t>(mat) * A.nparts + part] = t;
+  }
+}
+
+template <int MODE, int GDT>
+cudaError_t launch_mode(const PrologueArgs& a, cudaStream_t s) {
+  const dim3 grid(a.nparts, a.batch);
+  if (a.r > a.c)
+    prologue_kernel<MODE, GDT, true><<<grid, 256, 0, s>>>(a);
+  else
+    prologue_kernel<MODE, GDT, false><<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prologue(const PrologueArgs& a, int mode, int gdt, cudaStream_t s) {
+  const bool bf = (gdt == MUON_BF16);
+  switch (mode) {
+    case kPrologueNsOnly:
+      return bf ? launch_mode<kPrologueNsOnly, MUON_BF16>(a, s)
+                : launch_mode<kPrologueNsOnly, MUON_F32>(a, s);
+    case kPrologueNesterov:
+      return bf ? launch_mode<kPrologueNesterov, MUON_BF16>(a, s)
+                : launch_mode<kPrologueNesterov, MUON_F32>(a, s);
+    case kProloguePlain:
+      return bf ? launch_mode<kProloguePlain, MUON_BF16>(a, s)
+                : launch_mode<kProloguePlain, MUON_F32>(a, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace muon

@@ -1,0 +1,285 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU float64 oracle.
+
+Tolerances (per matrix, relative Frobenius):
+  * bf16 tensor-core NS (min(rows,cols) >= 64):  3e-2
+  * fp32 small-matrix NS (min(rows,cols) < 64):   1e-4
+  * fp32 elementwise momentum buffer:             1e-5
+  * the parameter write is checked as its update  p - (1 - lr wd) p0  against
+    -lr s O_ref (NS tolerance), so a small update cannot hide NS error, and the
+    pure decay part (zero gradient) exactly to 1e-6.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import newton_schulz_step_gb300 as muon
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+NS_TOL = 3e-2
+SMALL_TOL = 1e-4
+EW_TOL = 1e-5
+DEV = "cuda"
+
+
+def rel(x, ref):
+    den = np.linalg.norm(ref)
+    return np.linalg.norm(x - ref) / (den if den > 0 else 1.0)
+
+
+def f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def ns_tol(r, c):
+    return SMALL_TOL if min(r, c) < 64 else NS_TOL
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    muon.load_library()
+    yield
+    torch.cuda.synchronize()
+
+
+def _rand(shape, std, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(*shape, generator=g) * std).to(dtype)
+
+
+# ------------------------------------------------------------ intermediate buffers
+@pytest.mark.parametrize("shape,gdt", [((2, 256, 384), torch.bfloat16),
+                                       ((1, 300, 520), torch.float32),
+                                       ((2, 520, 300), torch.bfloat16)])
+def test_prologue_writes_u_then_gram_and_poly(shape, gdt):
+    """steps=1 leaves X0 = bf16(u or u^T), A = s^2 X0 X0^T and B = bA + cA^2 in the workspace."""
+    b, r, c = shape
+    m, n = min(r, c), max(r, c)
+    ldx, lda = (n + 7) // 8 * 8, (m + 7) // 8 * 8
+    g = _rand(shape, 1e-3, gdt, 1)
+    p = _rand(shape, 0.02, torch.float32, 2)
+    m0 = _rand(shape, 1e-3, torch.float32, 3)
+    need = muon.workspace_bytes(b, r, c)
+    ws = muon.Workspace(need)
+    pg, gg, mg = p.to(DEV), g.to(DEV), m0.to(DEV)
+    muon.step(pg, gg, mg, momentum=0.9, lr=0.02, weight_decay=0.01, steps=1, workspace=ws)
+    torch.cuda.synchronize()
+    assert muon.workspace_status(ws) == 0
+    raw = ws.tensor
+    x0_bytes = b * m * ldx * 2
+    a_off = 256 + 2 * ((x0_bytes + 255) // 256 * 256)
+    X0 = raw[256:256 + x0_bytes].view(torch.bfloat16).view(b, m, ldx)[:, :, :n]
+    A = raw[a_off:a_off + b * m * lda * 2].view(torch.bfloat16).view(b, m, lda)[:, :, :m]
+    a_bytes = (b * m * lda * 2 + 255) // 256 * 256
+    Bm = raw[a_off + a_bytes:a_off + a_bytes + b * m * lda * 2].view(torch.bfloat16).view(b, m, lda)[:, :, :m]
+    for i in range(b):
+        buf = oracle.momentum_buffer_update(f64(m0[i]), f64(g[i]), 0.9)
+        u = oracle.nesterov_blend(f64(g[i]), buf, 0.9)
+        X = u.T if r > c else u
+        assert rel(f64(mg[i]), buf) < EW_TOL
+        assert rel(f64(X0[i]), X) < 8e-3        # one bf16 rounding
+        x = f64(X0[i])
+        s = 1.0 / (np.linalg.norm(u) + 1e-7)
+        A_ref = s * s * (x @ x.T)
+        assert rel(f64(A[i]), A_ref) < 8e-3
+        a_ = f64(A[i])
+        B_ref = muon.COEFFS[1] * a_ + muon.COEFFS[2] * (a_ @ a_)
+        assert rel(f64(Bm[i]), B_ref) < 2e-2
+
+
+# ------------------------------------------------------------ NS only
+NS_SHAPES = [(1, 64, 64), (2, 128, 256), (2, 256, 128), (3, 300, 520), (2, 520, 300),
+             (1, 768, 768), (2, 129, 1000), (1, 200, 200), (1, 65, 67), (1, 1000, 129),
+             (1, 1, 12), (4, 12, 768), (2, 768, 12), (1, 63, 100), (1, 5, 5), (2, 1, 1)]
+
+
+@pytest.mark.parametrize("shape", NS_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("gdt", [torch.bfloat16, torch.float32])
+def test_ns5_matches_oracle(shape, gdt):
+    b, r, c = shape
+    G = _rand(shape, 1.0, gdt, 7 + r + c)
+    out = muon.ns5(G.to(DEV))
+    torch.cuda.synchronize()
+    for i in range(b):
+        ref = oracle.newton_schulz5(f64(G[i]))
+        err = rel(f64(out[i]), ref)
+        # the bf16 output adds one rounding (~2e-3) on top of the iteration error
+        tol = NS_TOL if min(r, c) >= 64 else 5e-3
+        assert err < tol, f"matrix {i}: rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("steps", [1, 2, 3, 7])
+def test_ns5_other_round_counts(steps):
+    G = _rand((2, 192, 320), 1.0, torch.bfloat16, 11)
+    out = muon.ns5(G.to(DEV), steps=steps)
+    torch.cuda.synchronize()
+    for i in range(2):
+        assert rel(f64(out[i]), oracle.newton_schulz5(f64(G[i]), steps=steps)) < NS_TOL
+
+
+def test_ns5_zero_matrix_gives_zero():
+    out = muon.ns5(torch.zeros(2, 128, 192, dtype=torch.bfloat16, device=DEV))
+    small = muon.ns5(torch.zeros(1, 8, 20, dtype=torch.bfloat16, device=DEV))
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out) == 0 and torch.count_nonzero(small) == 0
+
+
+def test_ns5_rank_one_closed_form(golden):
+    k = golden("poly_constants.txt")["p5_at_1"]
+    x = torch.randn(256, 1, dtype=torch.float64)
+    y = torch.randn(1, 384, dtype=torch.float64)
+    G = (x @ y).float()
+    out = muon.ns5(G.to(DEV))
+    torch.cuda.synchronize()
+    ref = k * G.double().numpy() / np.linalg.norm(G.double().numpy())
+    assert rel(f64(out), ref) < NS_TOL
+
+
+# ------------------------------------------------------------ full step, configs
+def _run_workload_and_check(wl, groups_dev, sample=None):
+    """groups_dev: list of (Group, P, G, B) on the GPU (not yet stepped)."""
+    before = []
+    for grp, P, G, B in groups_dev:
+        idx = sample(grp.batch) if sample else list(range(grp.batch))
+        before.append((idx, P[idx].cpu().clone(), G[idx].cpu().clone(), B[idx].cpu().clone()))
+    step = muon.GroupedStep([(P, G, B) for _, P, G, B in groups_dev], momentum=wl.momentum,
+                            lr=wl.lr, weight_decay=wl.weight_decay, nesterov=wl.nesterov,
+                            steps=wl.steps)
+    step()
+    torch.cuda.synchronize()
+    assert muon.workspace_status(step.workspace) == 0
+    decay = 1 - wl.lr * wl.weight_decay
+    worst = {}
+    for (grp, P, G, B), (idx, P0, G0, B0) in zip(groups_dev, before):
+        P1, B1 = P[idx].cpu(), B[idx].cpu()
+        for k, i in enumerate(idx):
+            p_ref, b_ref, o_ref = oracle.muon_step(
+                f64(P0[k]), f64(G0[k]), f64(B0[k]), momentum=wl.momentum, nesterov=wl.nesterov,
+                lr=wl.lr, weight_decay=wl.weight_decay, steps=wl.steps)
+            e_buf = rel(f64(B1[k]), b_ref)
+            upd = f64(P1[k]) - decay * f64(P0[k])
+            upd_ref = p_ref - decay * f64(P0[k])
+            e_upd = rel(upd, upd_ref)
+            worst[grp.name] = max(worst.get(grp.name, 0.0), e_upd)
+            assert e_buf < EW_TOL, f"{grp.name}[{i}] momentum buffer err {e_buf:.3e}"
+            assert e_upd < ns_tol(grp.rows, grp.cols), f"{grp.name}[{i}] update err {e_upd:.3e}"
+    return worst
+
+
+@pytest.mark.parametrize("name", ["cfg1", "cfg2", "cfg3"])
+def test_step_matches_oracle_on_small_workloads(name):
+    wl = workloads.get(name)
+    cpu = workloads.make_workload(wl, "cpu")       # CPU draws, copied byte for byte
+    dev = [(grp, P.to(DEV), G.to(DEV), B.to(DEV)) for grp, P, G, B in cpu]
+    worst = _run_workload_and_check(wl, dev)
+    print(name, {k: f"{v:.2e}" for k, v in worst.items()})
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["cfg4", "cfg5"])
+def test_step_matches_oracle_on_full_size_workloads_sampled(name):
+    """Full size, the same grouped call bench.py times; first/middle/last matrix of each group."""
+    wl = workloads.get(name)
+    dev = workloads.make_workload(wl, DEV)
+    worst = _run_workload_and_check(wl, dev, sample=workloads.sample_indices)
+    print(name, {k: f"{v:.2e}" for k, v in worst.items()})
+    del dev
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------ edge cases
+def test_zero_gradient_is_pure_decay_and_mixed_groups():
+    shapes = [(2, 96, 160), (1, 12, 40), (3, 200, 64)]
+    groups, p0s = [], []
+    for k, s in enumerate(shapes):
+        p = _rand(s, 0.02, torch.float32, 20 + k).to(DEV)
+        p0s.append(p.clone())
+        groups.append((p, torch.zeros(s, dtype=torch.bfloat16, device=DEV),
+                       torch.zeros(s, dtype=torch.float32, device=DEV)))
+    muon.step_grouped(groups, momentum=0.95, lr=0.02, weight_decay=0.01)
+    torch.cuda.synchronize()
+    for (p, _, b), p0 in zip(groups, p0s):
+        assert rel(f64(p), 0.9998 * f64(p0)) < 1e-6
+        assert torch.count_nonzero(b) == 0
+
+
+def test_empty_batch_and_empty_group_list_are_noops():
+    p = torch.zeros(0, 64, 64, device=DEV)
+    muon.step_grouped([(p, torch.zeros(0, 64, 64, dtype=torch.bfloat16, device=DEV),
+                        torch.zeros(0, 64, 64, device=DEV))], momentum=0.9, lr=0.1, weight_decay=0)
+    muon.step_grouped([], momentum=0.9, lr=0.1, weight_decay=0)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("nesterov,lr_scale", [(False, 0.0), (True, 1.5)])
+def test_step_options(nesterov, lr_scale):
+    s = (2, 320, 192)   # tall: default rescale would be sqrt(320/192)
+    P = _rand(s, 0.02, torch.float32, 31)
+    G = _rand(s, 1e-3, torch.bfloat16, 32)
+    B0 = _rand(s, 1e-3, torch.float32, 33)
+    pd, gd, bd = P.to(DEV), G.to(DEV), B0.to(DEV)
+    muon.step(pd, gd, bd, momentum=0.8, nesterov=nesterov, lr=0.05, weight_decay=0.1,
+              lr_scale=lr_scale)
+    torch.cuda.synchronize()
+    for i in range(2):
+        p_ref, b_ref, _ = oracle.muon_step(f64(P[i]), f64(G[i]), f64(B0[i]), momentum=0.8,
+                                           nesterov=nesterov, lr=0.05, weight_decay=0.1,
+                                           lr_scale=lr_scale)
+        assert rel(f64(bd[i]), b_ref) < EW_TOL
+        upd, upd_ref = f64(pd[i]) - 0.995 * f64(P[i]), p_ref - 0.995 * f64(P[i])
+        assert rel(upd, upd_ref) < NS_TOL
+
+
+def test_more_groups_than_one_launch_holds():
+    # 11 tensor-core groups of different shapes: several grouped launches per stage
+    shapes = [(1, 64 + 16 * k, 128 + 24 * k) for k in range(11)]
+    groups, ref = [], []
+    for k, s in enumerate(shapes):
+        P, G, B0 = (_rand(s, 0.02, torch.float32, 40 + k), _rand(s, 1e-3, torch.bfloat16, 60 + k),
+                    torch.zeros(s))
+        ref.append((P, G, B0))
+        groups.append((P.to(DEV), G.to(DEV), B0.to(DEV)))
+    muon.step_grouped(groups, momentum=0.95, lr=0.02, weight_decay=0.01)
+    torch.cuda.synchronize()
+    for (P, G, B0), (pd, _, _) in zip(ref, groups):
+        p_ref, _, _ = oracle.muon_step(f64(P[0]), f64(G[0]), f64(B0[0]), momentum=0.95, lr=0.02,
+                                       weight_decay=0.01)
+        upd, upd_ref = f64(pd[0]) - 0.9998 * f64(P[0]), p_ref - 0.9998 * f64(P[0])
+        assert rel(upd, upd_ref) < NS_TOL
+
+
+def test_deterministic_and_checkpoint_resume():
+    """Two runs give identical bits; step -> save -> load -> step equals two straight steps."""
+    wl = workloads.get("cfg2")
+    cpu = workloads.make_workload(wl, "cpu")
+
+    def fresh():
+        return [(P.to(DEV).clone(), G.to(DEV).clone(), B.to(DEV).clone()) for _, P, G, B in cpu]
+
+    kw = dict(momentum=wl.momentum, lr=wl.lr, weight_decay=wl.weight_decay)
+    a, b = fresh(), fresh()
+    sa, sb = muon.GroupedStep(a, **kw), muon.GroupedStep(b, **kw)
+    sa(), sa()
+    sb()
+    torch.cuda.synchronize()
+    state = [(p.cpu().clone(), m.cpu().clone()) for p, _, m in b]          # checkpoint
+    c = [(p.to(DEV), g, m.to(DEV)) for (p, m), (_, g, _) in zip(state, b)]  # resume elsewhere
+    muon.GroupedStep(c, **kw)()
+    torch.cuda.synchronize()
+    for (pa, _, ma), (pc, _, mc) in zip(a, c):
+        assert torch.equal(pa, pc) and torch.equal(ma, mc)
+
+
+def test_launch_count_and_trace():
+    G = _rand((2, 256, 256), 1.0, torch.bfloat16, 5).to(DEV)
+    n0 = muon.kernel_launch_count()
+    muon.trace_begin(64)
+    muon.ns5(G)
+    recs = muon.trace_end()
+    assert muon.kernel_launch_count() - n0 == 1 + 3 * 5
+    kinds = [r["kind"] for r in recs]
+    assert kinds[0] == "prologue" and kinds[-1] == "update_apply"
+    assert all(r["ms"] > 0 for r in recs)
