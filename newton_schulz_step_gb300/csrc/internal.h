@@ -14,9 +14,11 @@ namespace muon {
 constexpr int kTileM = 128;       // GEMM tile rows (UMMA M)
 constexpr int kTileK = 64;        // bf16 elements per 128-byte swizzle row
 constexpr int kSmallMaxM = 63;    // min(rows, cols) below 64 takes the fp32 path
-constexpr int kMaxParts = 32;     // norm partial sums per matrix
+constexpr int kMaxParts = 256;    // norm partial sums per matrix
 constexpr int kMaxProblems = 8;   // groups per grouped GEMM launch
 constexpr int kMaxSmallGroups = 16;
+constexpr int kMaxPrologueGroups = 16;
+constexpr int kSmallSmemFloats = 40960;  // X of a small matrix kept in shared memory up to 160 KB
 
 // Bits of the sticky device error word (first word of the workspace).
 enum DeviceError : unsigned int {
@@ -33,14 +35,24 @@ enum PrologueMode : int {
   kProloguePlain = 2,        // buf <- lerp(buf, g, 1-beta); u = buf
 };
 
-struct PrologueArgs {
+// One tensor-core group of the grouped prologue launch.
+struct PrologueGroup {
   const void* g;          // [batch, r, c] fp32 or bf16
   float* buf;             // [batch, r, c] fp32 (unused in kPrologueNsOnly)
   __nv_bfloat16* x;       // [batch, m, ldx] bf16: u, or u^T when r > c
   float* parts;           // [batch, nparts] partial sums of u^2
+  int gdt;
   int batch, r, c, ldx;
   int nparts;             // blocks per matrix (<= kMaxParts)
+  int block_begin;        // first block of this group in the launch
+};
+
+struct PrologueLaunch {
+  PrologueGroup grp[kMaxPrologueGroups];
+  int n_groups;
+  int total_blocks;
   float beta;
+  int wait_prior;         // 1: wait for the preceding grid (PDL) before exiting
 };
 
 // One group of the fp32 small-matrix path.
@@ -59,6 +71,7 @@ struct SmallGroup {
 struct SmallLaunch {
   SmallGroup grp[kMaxSmallGroups];
   int n_groups;
+  int x_in_smem;          // 1: X lives in dynamic shared memory (m*n <= kSmallSmemFloats)
   int mode;               // PrologueMode
   int steps;
   float beta, a, b, c, eps, decay;
@@ -102,8 +115,11 @@ enum GemmStage : int { kStageGram = 0, kStagePoly = 1, kStageUpdate = 2 };
 
 // Launchers (defined next to their kernels).  Each returns a cudaError_t from
 // the launch; grid sizes come from the caller's SM count.
-cudaError_t launch_prologue(const PrologueArgs& a, int mode, int gdt, cudaStream_t s);
-cudaError_t launch_small(const SmallLaunch& l, int total_blocks, cudaStream_t s);
+// The prologue may be launched as a programmatic dependent of the kernel
+// before it (pdl = true): it then overlaps that kernel and waits for it only
+// before exiting.
+cudaError_t launch_prologue(const PrologueLaunch& l, int mode, bool pdl, cudaStream_t s);
+cudaError_t launch_small(const SmallLaunch& l, int total_blocks, int max_mn, cudaStream_t s);
 cudaError_t launch_gemm(const GemmLaunch& l, int stage, int bn, int grid, cudaStream_t s);
 int gemm_smem_bytes(int stage, int bn);
 

@@ -186,8 +186,9 @@ size_t plan_workspace(std::vector<GPlan>& gs) {
       g.x1 = off; off += xb;
       g.am = off; off += ab;
       g.bm = off; off += ab;
+      // ~4 of the prologue's 64x64 tiles per block, at most kMaxParts blocks per matrix
       const int tiles = cdiv(g.r, 64) * cdiv(g.c, 64);
-      g.nparts = std::min(tiles, kMaxParts);
+      g.nparts = std::min(std::max(1, cdiv(tiles, 4)), kMaxParts);
       g.parts = off;
       off += align256(b * g.nparts * sizeof(float));
     }
@@ -350,7 +351,9 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
   if (s != MUON_OK) return s;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
 
-  // -- small matrices: one fp32 kernel for all of them
+  // -- small matrices: one fp32 kernel for all of them, launched first; it lets
+  //    the grouped prologue below start at once and run beside it
+  bool small_launched = false;
   {
     SmallLaunch sl;
     std::memset(&sl, 0, sizeof(sl));
@@ -362,17 +365,20 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
     sl.c = sc.c;
     sl.eps = sc.eps;
     sl.decay = 1.0f - sc.lr * sc.wd;
-    int blocks = 0;
+    int blocks = 0, max_mn = 0;
     auto flush = [&]() -> muon_status {
       if (sl.n_groups == 0) return MUON_OK;
       double bytes = 0;
       for (int i = 0; i < sl.n_groups; ++i)
         bytes += static_cast<double>(sl.grp[i].batch) * sl.grp[i].r * sl.grp[i].c *
                  (sc.mode == kPrologueNsOnly ? 6.0 : 20.0);
+      sl.x_in_smem = max_mn <= kSmallSmemFloats ? 1 : 0;
       const cudaError_t e = tracked_launch(st, {MUON_K_SMALL_NS, -1, 0.0, bytes},
-                                           [&] { return launch_small(sl, blocks, st); });
+                                           [&] { return launch_small(sl, blocks, max_mn, st); });
       sl.n_groups = 0;
       blocks = 0;
+      max_mn = 0;
+      small_launched = true;
       return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
     };
     for (GPlan& g : gs) {
@@ -393,6 +399,7 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
                                                   1.0, static_cast<double>(g.r) / g.c)));
       sg.lr_eff = sc.lr * scale;
       blocks += g.batch;
+      max_mn = std::max(max_mn, g.m * g.n);
       if (sl.n_groups == kMaxSmallGroups) {
         s = flush();
         if (s != MUON_OK) return s;
@@ -402,28 +409,39 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
     if (s != MUON_OK) return s;
   }
 
-  // -- tensor-core matrices
+  // -- tensor-core matrices: one grouped prologue launch (per kMaxPrologueGroups)
   std::vector<GPlan*> big;
   for (GPlan& g : gs)
     if (!g.small && g.batch > 0) big.push_back(&g);
-  for (GPlan* gp : big) {
-    const GPlan& g = *gp;
-    PrologueArgs pa;
-    pa.g = g.g;
-    pa.buf = g.buf;
-    pa.x = reinterpret_cast<__nv_bfloat16*>(ws + g.x0);
-    pa.parts = reinterpret_cast<float*>(ws + g.parts);
-    pa.batch = g.batch;
-    pa.r = g.r;
-    pa.c = g.c;
-    pa.ldx = g.ldx;
-    pa.nparts = g.nparts;
-    pa.beta = sc.beta;
-    const double elems = static_cast<double>(g.batch) * g.r * g.c;
-    const double bytes = elems * ((g.gdt == MUON_BF16 ? 2.0 : 4.0) + 2.0 +
-                                  (sc.mode == kPrologueNsOnly ? 0.0 : 8.0));
+  for (size_t c0 = 0; c0 < big.size(); c0 += kMaxPrologueGroups) {
+    PrologueLaunch pl;
+    std::memset(&pl, 0, sizeof(pl));
+    pl.beta = sc.beta;
+    double bytes = 0;
+    int blocks = 0;
+    for (size_t k = c0; k < std::min(big.size(), c0 + kMaxPrologueGroups); ++k) {
+      const GPlan& g = *big[k];
+      PrologueGroup& pg = pl.grp[pl.n_groups++];
+      pg.g = g.g;
+      pg.buf = g.buf;
+      pg.x = reinterpret_cast<__nv_bfloat16*>(ws + g.x0);
+      pg.parts = reinterpret_cast<float*>(ws + g.parts);
+      pg.gdt = g.gdt;
+      pg.batch = g.batch;
+      pg.r = g.r;
+      pg.c = g.c;
+      pg.ldx = g.ldx;
+      pg.nparts = g.nparts;
+      pg.block_begin = blocks;
+      blocks += g.batch * g.nparts;
+      bytes += static_cast<double>(g.batch) * g.r * g.c *
+               ((g.gdt == MUON_BF16 ? 2.0 : 4.0) + 2.0 + (sc.mode == kPrologueNsOnly ? 0.0 : 8.0));
+    }
+    pl.total_blocks = blocks;
+    const bool pdl = small_launched && c0 == 0;
+    pl.wait_prior = pdl ? 1 : 0;
     const cudaError_t e = tracked_launch(st, {MUON_K_PROLOGUE, -1, 0.0, bytes},
-                                         [&] { return launch_prologue(pa, sc.mode, g.gdt, st); });
+                                         [&] { return launch_prologue(pl, sc.mode, pdl, st); });
     if (e != cudaSuccess) return MUON_ERR_CUDA;
   }
 

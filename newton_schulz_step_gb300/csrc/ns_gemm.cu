@@ -205,71 +205,166 @@ __device__ __forceinline__ float inv_fro_norm(const float* parts, int nparts, fl
   return 1.0f / (sqrtf(acc) + eps);
 }
 
-__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float (&f)[32]) {
-  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+// bf16 halves of a packed pair as floats (bf16 is the top half of an fp32).
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// 32 consecutive bf16 of a row (zero past `valid`), kept packed.
+__device__ __forceinline__ void load_row32(const __nv_bfloat16* src, int valid,
+                                           uint32_t (&w)[16]) {
+  if (valid >= 32) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 w = s4[q];
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = s4[q];
+      w[4 * q + 0] = v.x;
+      w[4 * q + 1] = v.y;
+      w[4 * q + 2] = v.z;
+      w[4 * q + 3] = v.w;
+    }
+  } else {
+    const unsigned short* h = reinterpret_cast<const unsigned short*>(src);
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&ws[h]);
-      float2 f2 = __bfloat1622float2(b2);
-      f[q * 8 + 2 * h] = f2.x;
-      f[q * 8 + 2 * h + 1] = f2.y;
+    for (int t = 0; t < 16; ++t) {
+      const uint32_t lo = (2 * t < valid) ? h[2 * t] : 0u;
+      const uint32_t hi = (2 * t + 1 < valid) ? h[2 * t + 1] : 0u;
+      w[t] = lo | (hi << 16);
     }
   }
 }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&f)[32]) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, int valid, const float (&f)[32]) {
+  if (valid >= 32) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t ws[4];
+    for (int q = 0; q < 4; ++q) {
+      uint32_t ws[4];
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      __nv_bfloat162 b2 = __floats2bfloat162_rn(f[q * 8 + 2 * h], f[q * 8 + 2 * h + 1]);
-      ws[h] = *reinterpret_cast<uint32_t*>(&b2);
+      for (int h = 0; h < 4; ++h) {
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(f[q * 8 + 2 * h], f[q * 8 + 2 * h + 1]);
+        ws[h] = *reinterpret_cast<uint32_t*>(&b2);
+      }
+      d4[q] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
     }
-    d4[q] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+  } else {
+#pragma unroll
+    for (int t = 0; t < 32; ++t)
+      if (t < valid) dst[t] = __float2bfloat16_rn(f[t]);
   }
 }
 
-// Gram / Poly tile epilogue: row i of the output, columns j0..j0+31.
+// Parameter values the apply epilogue of chunk (i, j0) overwrites.  Not tall:
+// p[i][j0..j0+31] of a [m, n] matrix; tall: p[j0+t][i] of an [n, m] matrix
+// (lanes hold consecutive i, so each access is coalesced across the warp).
+__device__ __forceinline__ void load_params32(const GemmProblem& P, int mat, int i, int j0,
+                                              float (&pv)[32]) {
+  const int m = P.m, n = P.n;
+  const size_t moff = static_cast<size_t>(mat) * m * n;
+  const int valid = n - j0;
+  if (!P.tall) {
+    const float* pr = P.param + moff + static_cast<size_t>(i) * n + j0;
+    if (valid >= 32 && (n & 3) == 0) {
+      const float4* p4 = reinterpret_cast<const float4*>(pr);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 w = p4[q];
+        pv[4 * q + 0] = w.x;
+        pv[4 * q + 1] = w.y;
+        pv[4 * q + 2] = w.z;
+        pv[4 * q + 3] = w.w;
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < 32; ++t) pv[t] = (t < valid) ? pr[t] : 0.f;
+    }
+  } else {
+    const float* pc = P.param + moff + static_cast<size_t>(j0) * m + i;
+#pragma unroll
+    for (int t = 0; t < 32; ++t) pv[t] = (t < valid) ? pc[static_cast<size_t>(t) * m] : 0.f;
+  }
+}
+
+// Final output of chunk (i, j0) in the input's orientation: the parameter
+// write p <- decay p - lr_eff x (kOutParam) or a bf16 copy of x (kOutBf16).
+__device__ __forceinline__ void store_output32(const GemmProblem& P, int mat, int i, int j0,
+                                               const float (&x)[32], const float (&pv)[32]) {
+  const int m = P.m, n = P.n;
+  const size_t moff = static_cast<size_t>(mat) * m * n;
+  const int valid = n - j0;
+  float o[32];
+  if (P.out_mode == kOutParam) {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) o[t] = fmaf(-P.lr_eff, x[t], P.decay * pv[t]);
+  } else {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) o[t] = x[t];
+  }
+  if (!P.tall) {
+    const size_t base = moff + static_cast<size_t>(i) * n + j0;
+    if (P.out_mode == kOutParam) {
+      float* pr = P.param + base;
+      if (valid >= 32 && (n & 3) == 0) {
+        float4* p4 = reinterpret_cast<float4*>(pr);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          p4[q] = make_float4(o[4 * q + 0], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (t < valid) pr[t] = o[t];
+      }
+    } else {
+      __nv_bfloat16* orow = P.out + base;
+      if (valid >= 32 && (n & 7) == 0) {
+        store_row32(orow, 32, o);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (t < valid) orow[t] = __float2bfloat16_rn(o[t]);
+      }
+    }
+  } else {
+    const size_t base = moff + static_cast<size_t>(j0) * m + i;
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      if (t < valid) {
+        if (P.out_mode == kOutParam)
+          P.param[base + static_cast<size_t>(t) * m] = o[t];
+        else
+          P.out[base + static_cast<size_t>(t) * m] = __float2bfloat16_rn(o[t]);
+      }
+    }
+  }
+}
+
+// Gram / Poly chunk: row i, columns j0..j0+31 of the symmetric output; stores
+// the entries on/above the diagonal directly and those above it mirrored.
 template <int STAGE>
 __device__ __forceinline__ void epilogue_sym_chunk(const GemmLaunch& L, const GemmProblem& P,
                                                    int mat, int i, int j0, float scale,
-                                                   const uint32_t (&v)[32]) {
+                                                   const uint32_t (&v)[32],
+                                                   const uint32_t (&av)[16]) {
   const int m = P.m, ld = P.lda;
   __nv_bfloat16* out = P.sym_out + static_cast<size_t>(mat) * m * ld;
   float val[32];
-  const bool full_chunk = (j0 + 32 <= m);
   if (STAGE == kStageGram) {
 #pragma unroll
     for (int t = 0; t < 32; ++t) val[t] = __uint_as_float(v[t]) * scale;
   } else {
-    const __nv_bfloat16* am = P.a_mat + static_cast<size_t>(mat) * m * ld +
-                              static_cast<size_t>(i) * ld + j0;
-    float av[32];
-    if (full_chunk) {
-      load_bf16x32(am, av);
-    } else {
 #pragma unroll
-      for (int t = 0; t < 32; ++t) av[t] = (j0 + t < m) ? __bfloat162float(am[t]) : 0.f;
+    for (int t = 0; t < 16; ++t) {
+      val[2 * t] = fmaf(L.c, __uint_as_float(v[2 * t]), L.b * bf_lo(av[t]));
+      val[2 * t + 1] = fmaf(L.c, __uint_as_float(v[2 * t + 1]), L.b * bf_hi(av[t]));
     }
-#pragma unroll
-    for (int t = 0; t < 32; ++t) val[t] = fmaf(L.c, __uint_as_float(v[t]), L.b * av[t]);
   }
-  // direct store of the entries on/above the diagonal
   __nv_bfloat16* orow = out + static_cast<size_t>(i) * ld + j0;
-  if (full_chunk && j0 >= i) {
-    store_bf16x32(orow, val);
+  if (j0 + 32 <= m && j0 >= i) {
+    store_row32(orow, 32, val);
   } else {
 #pragma unroll
     for (int t = 0; t < 32; ++t)
       if (j0 + t >= i && j0 + t < m) orow[t] = __float2bfloat16_rn(val[t]);
   }
-  // mirrored store of the entries strictly above the diagonal: A[j][i]
 #pragma unroll
   for (int t = 0; t < 32; ++t) {
     const int j = j0 + t;
@@ -277,87 +372,10 @@ __device__ __forceinline__ void epilogue_sym_chunk(const GemmLaunch& L, const Ge
   }
 }
 
-// Update tile epilogue: row i of X', columns j0..j0+31.
-__device__ __forceinline__ void epilogue_update_chunk(const GemmLaunch& L, const GemmProblem& P,
-                                                      int mat, int i, int j0, float s,
-                                                      const uint32_t (&v)[32]) {
-  const int m = P.m, n = P.n, ldx = P.ldx;
-  const bool full_chunk = (j0 + 32 <= n);
-  const __nv_bfloat16* xrow =
-      P.x_cur + static_cast<size_t>(mat) * m * ldx + static_cast<size_t>(i) * ldx + j0;
-  float xv[32];
-  if (full_chunk) {
-    load_bf16x32(xrow, xv);
-  } else {
-#pragma unroll
-    for (int t = 0; t < 32; ++t) xv[t] = (j0 + t < n) ? __bfloat162float(xrow[t]) : 0.f;
-  }
-  float val[32];
-#pragma unroll
-  for (int t = 0; t < 32; ++t) val[t] = s * fmaf(L.a, xv[t], __uint_as_float(v[t]));
-
-  if (P.out_mode == kOutX) {
-    __nv_bfloat16* orow =
-        P.x_next + static_cast<size_t>(mat) * m * ldx + static_cast<size_t>(i) * ldx + j0;
-    if (full_chunk) {
-      store_bf16x32(orow, val);
-    } else {
-#pragma unroll
-      for (int t = 0; t < 32; ++t)
-        if (j0 + t < n) orow[t] = __float2bfloat16_rn(val[t]);
-    }
-    return;
-  }
-  const size_t moff = static_cast<size_t>(mat) * m * n;
-  if (!P.tall) {
-    // output [rows=m, cols=n]: this thread owns 32 consecutive entries of row i
-    const size_t base = moff + static_cast<size_t>(i) * n + j0;
-    if (P.out_mode == kOutParam) {
-      float* pr = P.param + base;
-      if (full_chunk && (n & 3) == 0) {
-        float4* p4 = reinterpret_cast<float4*>(pr);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float4 w = p4[q];
-          w.x = fmaf(-P.lr_eff, val[4 * q + 0], P.decay * w.x);
-          w.y = fmaf(-P.lr_eff, val[4 * q + 1], P.decay * w.y);
-          w.z = fmaf(-P.lr_eff, val[4 * q + 2], P.decay * w.z);
-          w.w = fmaf(-P.lr_eff, val[4 * q + 3], P.decay * w.w);
-          p4[q] = w;
-        }
-      } else {
-#pragma unroll
-        for (int t = 0; t < 32; ++t)
-          if (j0 + t < n) pr[t] = fmaf(-P.lr_eff, val[t], P.decay * pr[t]);
-      }
-    } else {
-      __nv_bfloat16* orow = P.out + base;
-      if (full_chunk && (n & 7) == 0) {
-        store_bf16x32(orow, val);
-      } else {
-#pragma unroll
-        for (int t = 0; t < 32; ++t)
-          if (j0 + t < n) orow[t] = __float2bfloat16_rn(val[t]);
-      }
-    }
-  } else {
-    // transposed back: output [rows=n, cols=m], entry (j, i); lanes hold
-    // consecutive i, so each store instruction is coalesced across the warp
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      const int j = j0 + t;
-      if (j < n) {
-        const size_t idx = moff + static_cast<size_t>(j) * m + i;
-        if (P.out_mode == kOutParam)
-          P.param[idx] = fmaf(-P.lr_eff, val[t], P.decay * P.param[idx]);
-        else
-          P.out[idx] = __float2bfloat16_rn(val[t]);
-      }
-    }
-  }
-}
-
 // ------------------------------------------------------------ epilogue warps
+// Operands a chunk needs besides the accumulator are loaded one chunk ahead
+// (the first chunk before waiting for the accumulator), so their latency
+// overlaps the TMEM load and the previous chunk's math and stores.
 template <int STAGE, int BN>
 __device__ void run_epilogue(const GemmLaunch& L, uint64_t* acc_full, uint64_t* acc_empty,
                              uint32_t tmem_base, volatile int* abort_flag, int warp, int lane) {
@@ -372,6 +390,25 @@ __device__ void run_epilogue(const GemmLaunch& L, uint64_t* acc_full, uint64_t* 
     float s = 1.f;
     if (STAGE != kStagePoly && P.first_round)
       s = inv_fro_norm(P.parts + static_cast<size_t>(tl.mat) * P.nparts, P.nparts, L.eps, lane);
+    const int i = tl.tm * kTileM + row;
+    const bool row_ok = i < P.m;
+    const int ncols = (STAGE == kStageUpdate) ? P.n : P.m;
+    const bool need_e = (STAGE != kStageGram);
+    const bool need_p = (STAGE == kStageUpdate) && P.out_mode == kOutParam;
+    const size_t ld = (STAGE == kStageUpdate) ? P.ldx : P.lda;
+    const __nv_bfloat16* esrc =
+        (STAGE == kStageUpdate ? P.x_cur : P.a_mat) +
+        static_cast<size_t>(tl.mat) * P.m * ld + static_cast<size_t>(row_ok ? i : 0) * ld;
+
+    uint32_t e_cur[16], e_nxt[16];
+    float p_cur[32], p_nxt[32];
+    {
+      const int j0 = tl.tn * BN;
+      if (row_ok && j0 < ncols) {
+        if (need_e) load_row32(esrc + j0, ncols - j0, e_cur);
+        if (need_p) load_params32(P, tl.mat, i, j0, p_cur);
+      }
+    }
     const bool got = ptx::mbar_wait(&acc_full[acc], acc_phase, abort_flag);
     __syncwarp();
     if (!got) {
@@ -381,21 +418,42 @@ __device__ void run_epilogue(const GemmLaunch& L, uint64_t* acc_full, uint64_t* 
     ptx::tc_fence_after();
     const uint32_t tbase =
         tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
-    const int i = tl.tm * kTileM + row;
-    const int ncols = (STAGE == kStageUpdate) ? P.n : P.m;
 #pragma unroll 1
     for (int ch = 0; ch < BN / 32; ++ch) {
       const int j0 = tl.tn * BN + ch * 32;
       if (j0 >= ncols) break;  // warp-uniform
+      const int jn = j0 + 32;
+      if (row_ok && ch + 1 < BN / 32 && jn < ncols) {
+        if (need_e) load_row32(esrc + jn, ncols - jn, e_nxt);
+        if (need_p) load_params32(P, tl.mat, i, jn, p_nxt);
+      }
       __syncwarp();
       uint32_t v[32];
       ptx::tmem_ld32(tbase + static_cast<uint32_t>(ch * 32), v);
       ptx::tmem_ld_wait();
-      if (i < P.m) {
-        if (STAGE == kStageUpdate)
-          epilogue_update_chunk(L, P, tl.mat, i, j0, s, v);
-        else
-          epilogue_sym_chunk<STAGE>(L, P, tl.mat, i, j0, s * s, v);
+      if (row_ok) {
+        if (STAGE == kStageUpdate) {
+          float x[32];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            x[2 * q] = s * fmaf(L.a, bf_lo(e_cur[q]), __uint_as_float(v[2 * q]));
+            x[2 * q + 1] = s * fmaf(L.a, bf_hi(e_cur[q]), __uint_as_float(v[2 * q + 1]));
+          }
+          if (P.out_mode == kOutX)
+            store_row32(P.x_next + static_cast<size_t>(tl.mat) * P.m * P.ldx +
+                            static_cast<size_t>(i) * P.ldx + j0,
+                        ncols - j0, x);
+          else
+            store_output32(P, tl.mat, i, j0, x, p_cur);
+        } else {
+          epilogue_sym_chunk<STAGE>(L, P, tl.mat, i, j0, s * s, v, e_cur);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 16; ++q) e_cur[q] = e_nxt[q];
+      if (need_p) {
+#pragma unroll
+        for (int q = 0; q < 32; ++q) p_cur[q] = p_nxt[q];
       }
     }
     ptx::tc_fence_before();

@@ -10,6 +10,11 @@
 //   X = u (u^T if rows > cols) / (||u||_F + eps)                (m x n, fp32, workspace)
 //   steps x:  A = X X^T;  B = b A + c A A;  X = a X + B X       (A, B in shared memory)
 //   p <- (1 - lr wd) p - lr_eff X^(T)   or   out <- bf16(X^(T))
+//
+// X stays in dynamic shared memory when every small matrix of the launch fits
+// (m n <= kSmallSmemFloats), else in the fp32 workspace.  The kernel lets the
+// next grid in the stream (the grouped prologue) start at once: the two are
+// independent and run side by side.
 #include "internal.h"
 
 namespace muon {
@@ -31,12 +36,34 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
+// X = a X + B X for the columns owned by this thread; MP >= m bounds the
+// unrolled register column (B is zero-padded past m).
+template <int MP>
+__device__ __forceinline__ void update_columns(float* X, const float* Bs, int m, int n, float a) {
+  for (int k = threadIdx.x; k < n; k += kSmallThreads) {
+    float xv[MP];
+#pragma unroll
+    for (int l = 0; l < MP; ++l) xv[l] = (l < m) ? X[static_cast<size_t>(l) * n + k] : 0.f;
+    for (int i = 0; i < m; ++i) {
+      float acc = 0.f;
+#pragma unroll
+      for (int l = 0; l < MP; ++l) acc = fmaf(Bs[i * kSmallLd + l], xv[l], acc);
+      float* xi = X + static_cast<size_t>(i) * n + k;
+      *xi = fmaf(a, *xi, acc);
+    }
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kSmallThreads) small_ns_kernel(
     const __grid_constant__ SmallLaunch L) {
   __shared__ float As[kSmallLd * kSmallLd];
   __shared__ float Bs[kSmallLd * kSmallLd];
   __shared__ float red[kSmallThreads / 32];
+  extern __shared__ float xs_dyn[];
+
+  // the next grid (independent work) may start right away
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   int gi = 0;
   while (gi + 1 < L.n_groups && static_cast<int>(blockIdx.x) >= L.grp[gi + 1].block_begin) ++gi;
@@ -48,7 +75,7 @@ __global__ void __launch_bounds__(kSmallThreads) small_ns_kernel(
   const int n = tall ? r : c;
   const size_t moff = static_cast<size_t>(mat) * r * c;
   const int total = r * c;
-  float* X = G.x + moff;  // m x n, row-major
+  float* X = L.x_in_smem ? xs_dyn : G.x + moff;  // m x n, row-major
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const float beta = L.beta;
@@ -104,18 +131,12 @@ __global__ void __launch_bounds__(kSmallThreads) small_ns_kernel(
     }
     __syncthreads();
     // X = a X + B X, one column of X per thread (columns are independent)
-    for (int k = tid; k < n; k += kSmallThreads) {
-      float xv[kSmallLd];
-#pragma unroll
-      for (int l = 0; l < kSmallLd; ++l) xv[l] = (l < m) ? X[static_cast<size_t>(l) * n + k] : 0.f;
-      for (int i = 0; i < m; ++i) {
-        float acc = 0.f;
-#pragma unroll
-        for (int l = 0; l < kSmallLd; ++l) acc = fmaf(Bs[i * kSmallLd + l], xv[l], acc);
-        float* xi = X + static_cast<size_t>(i) * n + k;
-        *xi = fmaf(L.a, *xi, acc);
-      }
-    }
+    if (m <= 16)
+      update_columns<16>(X, Bs, m, n, L.a);
+    else if (m <= 32)
+      update_columns<32>(X, Bs, m, n, L.a);
+    else
+      update_columns<64>(X, Bs, m, n, L.a);
     __syncthreads();
   }
 
@@ -132,21 +153,35 @@ __global__ void __launch_bounds__(kSmallThreads) small_ns_kernel(
 
 }  // namespace
 
-cudaError_t launch_small(const SmallLaunch& l, int total_blocks, cudaStream_t s) {
+cudaError_t launch_small(const SmallLaunch& l, int total_blocks, int max_mn, cudaStream_t s) {
+  const size_t smem = l.x_in_smem ? static_cast<size_t>(max_mn) * sizeof(float) : 0;
+  // static A, B (32 KB) plus up to 160 KB of X: above the 48 KB default, so
+  // the limit is raised once per device and kernel instance
+  static int configured[3][64] = {{0}};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  auto run = [&](auto kern, int which) -> cudaError_t {
+    if (dev >= 64 || !configured[which][dev]) {
+      const cudaError_t ea =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kSmallSmemFloats * sizeof(float)));
+      if (ea != cudaSuccess) return ea;
+      if (dev < 64) configured[which][dev] = 1;
+    }
+    kern<<<total_blocks, kSmallThreads, smem, s>>>(l);
+    return cudaGetLastError();
+  };
   switch (l.mode) {
     case kPrologueNsOnly:
-      small_ns_kernel<kPrologueNsOnly><<<total_blocks, kSmallThreads, 0, s>>>(l);
-      break;
+      return run(small_ns_kernel<kPrologueNsOnly>, 0);
     case kPrologueNesterov:
-      small_ns_kernel<kPrologueNesterov><<<total_blocks, kSmallThreads, 0, s>>>(l);
-      break;
+      return run(small_ns_kernel<kPrologueNesterov>, 1);
     case kProloguePlain:
-      small_ns_kernel<kProloguePlain><<<total_blocks, kSmallThreads, 0, s>>>(l);
-      break;
+      return run(small_ns_kernel<kProloguePlain>, 2);
     default:
       return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace muon

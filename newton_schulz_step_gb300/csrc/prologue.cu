@@ -11,20 +11,22 @@
 // ||u||_F + eps is folded into the first Gram and update epilogues, which sum
 // the partials in a fixed order, so the result is deterministic.
 //
-// Grid: (nparts, batch); block b of matrix z walks the 64x64 tiles
-// b, b + nparts, ... of that matrix.  Each thread moves 2 x 8 consecutive
-// elements of a tile row with 16-byte accesses; rows > cols tiles are
-// transposed through shared memory so the X stores stay coalesced.
+// One launch covers every tensor-core group: block b of the launch belongs to
+// group g, matrix z, part q, and walks the 64x64 tiles q, q + nparts, ... of
+// that matrix (nparts is chosen per group so each block gets ~4 tiles).  Each
+// thread moves 2 x 8 consecutive elements of a tile row with 16-byte accesses;
+// rows > cols tiles are transposed through shared memory so the X stores stay
+// coalesced.  Launched as a programmatic dependent of the small-matrix kernel,
+// it overlaps that kernel and waits for it only before exiting.
 #include "internal.h"
 
 namespace muon {
 
 namespace {
 
-template <int GDT>
-__device__ __forceinline__ void load_g8(const void* g, size_t idx, bool vec, int valid,
+__device__ __forceinline__ void load_g8(const void* g, int gdt, size_t idx, bool vec, int valid,
                                         float (&out)[8]) {
-  if (GDT == MUON_BF16) {
+  if (gdt == MUON_BF16) {
     const __nv_bfloat16* gp = static_cast<const __nv_bfloat16*>(g) + idx;
     if (vec) {
       const uint4 w = *reinterpret_cast<const uint4*>(gp);
@@ -93,23 +95,28 @@ __device__ __forceinline__ void store_bf8(__nv_bfloat16* p, bool vec, int valid,
   }
 }
 
-template <int MODE, int GDT, bool TALL>
-__global__ void __launch_bounds__(256) prologue_kernel(const PrologueArgs A) {
-  __shared__ float stage_tile[TALL ? 64 : 1][65];
+template <int MODE>
+__global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ PrologueLaunch L) {
+  __shared__ float stage_tile[64][65];
   __shared__ float red[8];
-  const int mat = blockIdx.y;
-  const int part = blockIdx.x;
+  int gi = 0;
+  while (gi + 1 < L.n_groups && static_cast<int>(blockIdx.x) >= L.grp[gi + 1].block_begin) ++gi;
+  const PrologueGroup& A = L.grp[gi];
+  const int local = blockIdx.x - A.block_begin;
+  const int mat = local / A.nparts;
+  const int part = local - mat * A.nparts;
   const int r = A.r, c = A.c;
+  const bool tall = r > c;
   const int tiles_c = (c + 63) / 64;
   const int ntiles = ((r + 63) / 64) * tiles_c;
   const size_t moff = static_cast<size_t>(mat) * r * c;
-  const int m = TALL ? c : r;
+  const int m = tall ? c : r;
   __nv_bfloat16* xm = A.x + static_cast<size_t>(mat) * m * A.ldx;
   const int tid = threadIdx.x;
   const int ty = tid >> 3;        // tile row within a 32-row half
   const int tx = (tid & 7) * 8;   // first of 8 tile columns
   const bool cvec = (c & 7) == 0; // rows start 16-byte aligned
-  const float beta = A.beta;
+  const float beta = L.beta;
   float sumsq = 0.f;
 
   for (int tile = part; tile < ntiles; tile += A.nparts) {
@@ -125,7 +132,7 @@ __global__ void __launch_bounds__(256) prologue_kernel(const PrologueArgs A) {
       const bool in = rr < r && valid > 0;
       const size_t idx = moff + static_cast<size_t>(rr) * c + cc;
       if (in) {
-        load_g8<GDT>(A.g, idx, cvec && valid == 8, valid, gv[h]);
+        load_g8(A.g, A.gdt, idx, cvec && valid == 8, valid, gv[h]);
         if (MODE != kPrologueNsOnly) load_f8(A.buf + idx, cvec && valid == 8, valid, bv[h]);
       } else {
 #pragma unroll
@@ -152,14 +159,14 @@ __global__ void __launch_bounds__(256) prologue_kernel(const PrologueArgs A) {
       }
 #pragma unroll
       for (int e = 0; e < 8; ++e) sumsq = fmaf(u[e], u[e], sumsq);
-      if (!TALL) {
+      if (!tall) {
         if (in) store_bf8(xm + static_cast<size_t>(rr) * A.ldx + cc, valid == 8, valid, u);
       } else {
 #pragma unroll
         for (int e = 0; e < 8; ++e) stage_tile[ty + 32 * h][tx + e] = u[e];
       }
     }
-    if (TALL) {
+    if (tall) {
       // X = u^T: X row (original column) tc*64 + ..., X columns tr*64 + ...
       __syncthreads();
       const int xc = tr * 64 + tx;                 // X column = original row
@@ -188,32 +195,35 @@ __global__ void __launch_bounds__(256) prologue_kernel(const PrologueArgs A) {
     for (int w = 0; w < 8; ++w) t += red[w];
     A.parts[static_cast<size_t>(mat) * A.nparts + part] = t;
   }
+  // Programmatic dependent of the small-matrix kernel: finish only after it.
+  if (L.wait_prior) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-template <int MODE, int GDT>
-cudaError_t launch_mode(const PrologueArgs& a, cudaStream_t s) {
-  const dim3 grid(a.nparts, a.batch);
-  if (a.r > a.c)
-    prologue_kernel<MODE, GDT, true><<<grid, 256, 0, s>>>(a);
-  else
-    prologue_kernel<MODE, GDT, false><<<grid, 256, 0, s>>>(a);
-  return cudaGetLastError();
+template <int MODE>
+cudaError_t launch_mode(const PrologueLaunch& l, bool pdl, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(l.total_blocks);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, prologue_kernel<MODE>, l);
 }
 
 }  // namespace
 
-cudaError_t launch_prologue(const PrologueArgs& a, int mode, int gdt, cudaStream_t s) {
-  const bool bf = (gdt == MUON_BF16);
+cudaError_t launch_prologue(const PrologueLaunch& l, int mode, bool pdl, cudaStream_t s) {
   switch (mode) {
     case kPrologueNsOnly:
-      return bf ? launch_mode<kPrologueNsOnly, MUON_BF16>(a, s)
-                : launch_mode<kPrologueNsOnly, MUON_F32>(a, s);
+      return launch_mode<kPrologueNsOnly>(l, pdl, s);
     case kPrologueNesterov:
-      return bf ? launch_mode<kPrologueNesterov, MUON_BF16>(a, s)
-                : launch_mode<kPrologueNesterov, MUON_F32>(a, s);
+      return launch_mode<kPrologueNesterov>(l, pdl, s);
     case kProloguePlain:
-      return bf ? launch_mode<kProloguePlain, MUON_BF16>(a, s)
-                : launch_mode<kProloguePlain, MUON_F32>(a, s);
+      return launch_mode<kProloguePlain>(l, pdl, s);
     default:
       return cudaErrorInvalidValue;
   }

@@ -60,7 +60,7 @@ def test_workspace_bytes(lib):
     # tensor-core path: X0, X1 (m x ldx bf16), A, B (m x lda bf16), norm partials
     b, r, c = 2, 300, 130          # tall: m = 130, n = 300
     m, n, ldx, lda = 130, 300, 304, 136
-    parts = min(5 * 3, 32)
+    parts = 4                      # ceil(15 prologue tiles / 4)
     expect = 256 + 2 * _align(b * m * ldx * 2) + 2 * _align(b * m * lda * 2) + _align(b * parts * 4)
     assert lib.muon_workspace_bytes(b, r, c) == expect
     # the grouped size is the sum of the per-group regions

@@ -127,15 +127,19 @@ def test_ns5_zero_matrix_gives_zero():
     assert torch.count_nonzero(out) == 0 and torch.count_nonzero(small) == 0
 
 
-def test_ns5_rank_one_closed_form(golden):
-    k = golden("poly_constants.txt")["p5_at_1"]
-    x = torch.randn(256, 1, dtype=torch.float64)
-    y = torch.randn(1, 384, dtype=torch.float64)
-    G = (x @ y).float()
-    out = muon.ns5(G.to(DEV))
+@pytest.mark.parametrize("m,n", [(128, 256), (768, 768)])
+def test_ns5_orthonormal_rows_closed_form(m, n, golden):
+    # G = k Q with orthonormal rows: every normalised singular value is 1/sqrt(m), so
+    # NS5(G) = p5(1/sqrt(m)) Q.  (A rank-deficient G is no test of the bf16 path: NS
+    # amplifies the bf16 rounding noise in the null space by up to a^5 ~ 487.)
+    k = golden("poly_constants.txt")[f"p5_at_inv_sqrt_{m}"]
+    q, _ = torch.linalg.qr(torch.randn(n, m, dtype=torch.float64, generator=torch.Generator().manual_seed(m)))
+    Q = q.T.contiguous()
+    out = muon.ns5((3.0 * Q).float().to(DEV))
+    out_t = muon.ns5((3.0 * Q.T).contiguous().float().to(DEV))
     torch.cuda.synchronize()
-    ref = k * G.double().numpy() / np.linalg.norm(G.double().numpy())
-    assert rel(f64(out), ref) < NS_TOL
+    assert rel(f64(out), k * Q.numpy()) < NS_TOL
+    assert rel(f64(out_t), k * Q.T.numpy()) < NS_TOL
 
 
 # ------------------------------------------------------------ full step, configs
