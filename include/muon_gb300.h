@@ -116,6 +116,25 @@ muon_status muon_step(float* params, const void* grads, int g_dtype, float* mome
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * muon_step without a workspace, for callers that cannot call cudaMalloc: code
+ * running under an allocator that has already reserved the whole GPU, plug-ins
+ * allowed to touch only the memory they are handed, or training loops that
+ * forbid any allocation after start-up.  The pages have no counterpart: this is
+ * an interface addition, not part of the method.
+ * Arguments and results are those of muon_step, minus the workspace.  Scratch is
+ * a 64 MiB array built into the library (held by every GPU that loads it until
+ * the process exits); a call whose muon_workspace_bytes(batch, rows, cols)
+ * exceeds 64 MiB returns MUON_ERR_WORKSPACE.  The first call on a device looks
+ * up the array's device address, so make it before any stream capture.  All
+ * calls on a device share the array: calls that overlap on the GPU race.
+ */
+muon_status muon_step_noalloc(float* params, const void* grads, int g_dtype, float* momentum_buf,
+                              int batch, int rows, int cols,
+                              float momentum, int nesterov, float lr, float weight_decay,
+                              float lr_scale, int steps, float a, float b, float c, float eps,
+                              void* stream);
+
+/*
  * muon_step on every group of a model at once (the pages stack the weights of
  * each parameter group, [MCS] 四 第一遍/第二遍).  Groups share the scalars; the
  * NS rounds of all tensor-core groups run as one grouped launch per stage.

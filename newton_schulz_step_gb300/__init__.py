@@ -21,7 +21,8 @@ import torch
 
 __all__ = [
     "COEFFS", "EPS", "MuonError", "load_library", "library_path", "workspace_bytes",
-    "grouped_workspace_bytes", "Workspace", "ns5", "step", "step_grouped", "GroupedStep",
+    "grouped_workspace_bytes", "Workspace", "ns5", "step", "step_noalloc", "step_grouped",
+    "GroupedStep",
     "workspace_status", "status_string", "kernel_launch_count", "trace_begin", "trace_end",
     "KERNEL_KINDS",
 ]
@@ -81,6 +82,9 @@ def load_library():
     L.muon_step.argtypes = [vp, vp, ci, vp, ci, ci, ci, cf, ci, cf, cf, cf, ci, cf, cf, cf, cf,
                             vp, sz, vp]
     L.muon_step.restype = ci
+    L.muon_step_noalloc.argtypes = [vp, vp, ci, vp, ci, ci, ci, cf, ci, cf, cf, cf, ci, cf, cf,
+                                    cf, cf, vp]
+    L.muon_step_noalloc.restype = ci
     L.muon_step_grouped.argtypes = [ctypes.POINTER(_Group), ci, cf, ci, cf, cf, ci, cf, cf, cf,
                                     cf, vp, sz, vp]
     L.muon_step_grouped.restype = ci
@@ -234,6 +238,24 @@ def step(params, grads, momentum_buf, *, momentum: float, lr: float, weight_deca
     _raise(L.muon_step(p3.data_ptr(), g3.data_ptr(), _gdt(g3), m3.data_ptr(), b, r, c,
                        momentum, int(bool(nesterov)), lr, weight_decay, lr_scale, steps,
                        a_, b_, c_, eps, ws.ptr, ws.nbytes, _stream_handle(stream)), "muon_step")
+
+
+def step_noalloc(params, grads, momentum_buf, *, momentum: float, lr: float,
+                 weight_decay: float, nesterov: bool = True, lr_scale: float = 0.0,
+                 steps: int = STEPS, coeffs=COEFFS, eps: float = EPS, stream=None):
+    """step() without a workspace, for callers that may not allocate device memory:
+    the library's built-in 64 MiB device scratch is used instead."""
+    L = load_library()
+    p3, g3, m3 = _as3d(params, "params"), _as3d(grads, "grads"), _as3d(momentum_buf, "momentum_buf")
+    if p3.dtype != torch.float32 or m3.dtype != torch.float32:
+        raise TypeError("params and momentum_buf must be float32")
+    if not (p3.shape == g3.shape == m3.shape):
+        raise ValueError("params, grads and momentum_buf must have the same shape")
+    b, r, c = g3.shape
+    a_, b_, c_ = coeffs
+    _raise(L.muon_step_noalloc(p3.data_ptr(), g3.data_ptr(), _gdt(g3), m3.data_ptr(), b, r, c,
+                               momentum, int(bool(nesterov)), lr, weight_decay, lr_scale, steps,
+                               a_, b_, c_, eps, _stream_handle(stream)), "muon_step_noalloc")
 
 
 def _normalise_groups(groups):
