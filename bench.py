@@ -292,7 +292,7 @@ def run_gpu(args, wl):
         k["n"] += 1
         k["flops"] += r["flops"]
         k["bytes"] += r["bytes"]
-    ns_kinds = ("gram", "poly", "update", "update_apply", "small_ns")
+    ns_kinds = ("gram", "poly", "update", "small_ns")
     ns_ms = sum(kinds[k]["ms"] for k in ns_kinds if k in kinds) / args.steps
     traced_ms = sum(k["ms"] for k in kinds.values()) / args.steps
     dom_name, dom = max(kinds.items(), key=lambda kv: kv[1]["ms"])
@@ -310,11 +310,18 @@ def run_gpu(args, wl):
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "traffic": traffic_for(dom_name, wl.name), "peak_source": peaks["source"],
                 "ms_per_launch": per_launch_ms, "bytes_per_launch": dom["bytes"] / dom["n"]}
-    pro = kinds.get("prologue")
-    prologue = None
-    if pro:
-        gbs = pro["bytes"] / (pro["ms"] / 1e3) / 1e9
-        prologue = {"gbs": gbs, "frac": gbs / peaks["hbm_gbs"], "ms_per_step": pro["ms"] / args.steps}
+    # elementwise kernels (HBM-bound): prologue and apply, bytes they must move
+    ew = [kinds[k] for k in ("prologue", "apply") if k in kinds]
+    elementwise = None
+    if ew:
+        ew_bytes = sum(k["bytes"] for k in ew)
+        ew_ms = sum(k["ms"] for k in ew)
+        gbs = ew_bytes / (ew_ms / 1e3) / 1e9
+        elementwise = {"gbs": gbs, "frac": gbs / peaks["hbm_gbs"],
+                       "ms_per_step": ew_ms / args.steps,
+                       "per_kernel": {name: {"gbs": kinds[name]["bytes"] / (kinds[name]["ms"] / 1e3) / 1e9,
+                                             "ms_per_step": kinds[name]["ms"] / args.steps}
+                                      for name in ("prologue", "apply") if name in kinds}}
 
     # end to end through the public API with host buffers: grads in, params out
     host_g = [G.cpu().pin_memory() for _, G, _ in tensors]
@@ -366,7 +373,7 @@ def run_gpu(args, wl):
             "traced_ms_per_step": traced_ms,
             "kernels": {k: {"ms_per_step": v["ms"] / args.steps, "launches_per_step":
                             v["n"] / args.steps} for k, v in kinds.items()},
-            "prologue": prologue,
+            "elementwise": elementwise,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clock,
         }

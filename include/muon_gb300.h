@@ -75,9 +75,9 @@ typedef enum muon_kernel_kind {
   MUON_K_PROLOGUE = 0,   /* momentum, Nesterov blend, bf16 cast, norm partials  */
   MUON_K_SMALL_NS = 1,   /* whole step in fp32 for min(rows,cols) < 64          */
   MUON_K_GRAM = 2,       /* A = s^2 X X^T, upper tiles + mirror                 */
-  MUON_K_POLY = 3,       /* B = b A + c A A, upper tiles + mirror               */
-  MUON_K_UPDATE = 4,     /* X <- s (a X + B X)                                  */
-  MUON_K_UPDATE_APPLY = 5/* last round: p <- (1-lr wd) p - lr scale (aX + BX)   */
+  MUON_K_POLY = 3,       /* B' = a I + b A + c A A, upper tiles + mirror        */
+  MUON_K_UPDATE = 4,     /* X <- s B' X  (= s (a X + B X))                      */
+  MUON_K_APPLY = 5       /* p <- (1 - lr wd) p - lr scale O (or O as bf16)      */
 } muon_kernel_kind;
 
 /* Workspace bytes for one muon_step()/muon_ns5() call on [batch, rows, cols].

@@ -32,8 +32,7 @@ COEFFS = (3.4445, -4.7750, 2.0315)
 STEPS = 5
 EPS = 1e-7
 
-KERNEL_KINDS = {0: "prologue", 1: "small_ns", 2: "gram", 3: "poly", 4: "update",
-                5: "update_apply"}
+KERNEL_KINDS = {0: "prologue", 1: "small_ns", 2: "gram", 3: "poly", 4: "update", 5: "apply"}
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "timeout",
            5: "workspace"}
 

@@ -55,6 +55,25 @@ struct PrologueLaunch {
   int wait_prior;         // 1: wait for the preceding grid (PDL) before exiting
 };
 
+// One tensor-core group of the grouped apply launch: the NS result O (bf16,
+// [batch, m, ldx], transposed when rows > cols) goes into the parameter,
+// p <- decay p - lr_eff O, or into a bf16 output, in the input's orientation.
+struct ApplyGroup {
+  const __nv_bfloat16* o;
+  float* param;
+  __nv_bfloat16* out;
+  int batch, r, c, ldx;
+  int nparts;
+  int block_begin;
+  float lr_eff, decay;
+};
+
+struct ApplyLaunch {
+  ApplyGroup grp[kMaxPrologueGroups];
+  int n_groups;
+  int total_blocks;
+};
+
 // One group of the fp32 small-matrix path.
 struct SmallGroup {
   const void* g;
@@ -77,36 +96,28 @@ struct SmallLaunch {
   float beta, a, b, c, eps, decay;
 };
 
-// Output of the last update round.
-enum OutMode : int { kOutX = 0, kOutParam = 1, kOutBf16 = 2 };
-
 struct GemmProblem {
   int batch, m, n;        // X is m x n (m <= n), batch matrices
   int ldx, lda;           // padded leading dimensions (elements) of X and A/B
-  int tiles_m, tiles_n;   // tile grid of this stage's output
-  int tiles_per_mat;
-  int tile_begin;         // first linear tile index of this problem
+  int tiles_m;            // pair rows: ceil(ceil(m / 128) / 2)
+  int tiles_n;            // 256-wide tile columns of this stage's output
+  int tiles_per_mat;      // pair tiles per matrix
+  int tile_begin;         // first linear pair-tile index of this problem
   int k_blocks;           // ceil(K / kTileK)
-  const __nv_bfloat16* x_cur;   // update: X of this round (a X term)
-  __nv_bfloat16* x_next;        // update: next X (kOutX)
   const __nv_bfloat16* a_mat;   // poly: A (b A term)
-  __nv_bfloat16* sym_out;       // gram: A, poly: B
   const float* parts;           // norm partials [batch, nparts]
   int nparts;
   int first_round;              // fold s = 1/(||u||_F + eps) in
-  int out_mode;                 // OutMode
-  int tall;                     // original rows > cols: outputs are transposed back
-  float* param;                 // kOutParam: [batch, rows, cols] fp32
-  __nv_bfloat16* out;           // kOutBf16: [batch, rows, cols]
-  float lr_eff, decay;
 };
 
 struct GemmLaunch {
-  CUtensorMap tm_a[kMaxProblems];   // operand A tiles (box 64 x 128)
-  CUtensorMap tm_b[kMaxProblems];   // operand B tiles
+  CUtensorMap tm_a[kMaxProblems];   // operand A tiles (box 64 x 128, 128-byte swizzle)
+  CUtensorMap tm_b[kMaxProblems];   // operand B half tiles (box 64 x 128, or 64 x 64 for X)
+  CUtensorMap tm_out[kMaxProblems]; // output blocks (box 32 x 32 bf16, 64-byte swizzle)
+  CUtensorMap tm_mir[kMaxProblems]; // mirrored output blocks (box 32 x 32 bf16, no swizzle)
   GemmProblem prob[kMaxProblems];
   int n_prob;
-  int total_tiles;
+  int total_tiles;                  // pair tiles
   float a, b, c, eps;
   unsigned int* status;             // sticky device error word
 };
@@ -120,7 +131,10 @@ enum GemmStage : int { kStageGram = 0, kStagePoly = 1, kStageUpdate = 2 };
 // before exiting.
 cudaError_t launch_prologue(const PrologueLaunch& l, int mode, bool pdl, cudaStream_t s);
 cudaError_t launch_small(const SmallLaunch& l, int total_blocks, int max_mn, cudaStream_t s);
-cudaError_t launch_gemm(const GemmLaunch& l, int stage, int bn, int grid, cudaStream_t s);
-int gemm_smem_bytes(int stage, int bn);
+cudaError_t launch_apply(const ApplyLaunch& l, bool to_param, cudaStream_t s);
+// One launch of a GEMM stage over `pair_tiles` cluster tiles (two 128 x 256
+// CTA tiles each); the grid is sized from the device's SM count.
+cudaError_t launch_gemm(const GemmLaunch& l, int stage, int pair_tiles, int sms, cudaStream_t s);
+int gemm_smem_bytes();
 
 }  // namespace muon

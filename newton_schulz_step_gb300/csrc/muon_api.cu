@@ -117,23 +117,36 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// bf16 [batch][rows][ld] with logical width `cols`; box = 64 columns x box_rows,
-// 128-byte swizzle, out-of-bounds elements read as zero.
+// bf16 [batch][rows][ld] with logical width `cols`; box = box_cols x box_rows x 1.
+// Loads read out-of-bounds elements as zero; stores skip them.
 bool make_tmap(CUtensorMap* tm, const void* base, int cols, int rows, int batch, int ld,
-               int box_rows) {
+               int box_cols, int box_rows, CUtensorMapSwizzle swizzle) {
   auto enc = get_encode();
   if (!enc) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(batch)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2,
                                  static_cast<cuuint64_t>(ld) * 2 * static_cast<cuuint64_t>(rows)};
-  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols),
+                             static_cast<cuuint32_t>(box_rows), 1u};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
-                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// GEMM operand tiles: 64 columns (128 bytes) x box_rows, 128-byte swizzle.
+bool operand_tmap(CUtensorMap* tm, const void* base, int cols, int rows, int batch, int ld,
+                  int box_rows) {
+  return make_tmap(tm, base, cols, rows, batch, ld, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Epilogue output blocks of 32 x 32: 64-byte swizzle (direct) or none (mirror).
+bool output_tmap(CUtensorMap* tm, const void* base, int cols, int rows, int batch, int ld,
+                 bool swizzled) {
+  return make_tmap(tm, base, cols, rows, batch, ld, 32, 32,
+                   swizzled ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // ------------------------------------------------------------ planning
@@ -237,18 +250,23 @@ struct StageShape {
   int tiles_m, tiles_n, tiles_per_mat, k_blocks;
 };
 
-StageShape stage_shape(const GPlan& g, int stage, int bn) {
+// Tiles of one stage in units of cluster pairs: two 128-row CTA tiles (rows
+// 2p, 2p+1) of one 256-wide column.  Symmetric stages take, for pair row p,
+// the columns q >= p (exactly the columns holding entries on or above the
+// diagonal for both rows of the pair).
+constexpr int kTileN = 256;
+
+StageShape stage_shape(const GPlan& g, int stage) {
   StageShape s{};
+  s.tiles_m = cdiv(cdiv(g.m, kTileM), 2);
   if (stage == kStageUpdate) {
-    s.tiles_m = cdiv(g.m, kTileM);
-    s.tiles_n = cdiv(g.n, bn);
+    s.tiles_n = cdiv(g.n, kTileN);
     s.tiles_per_mat = s.tiles_m * s.tiles_n;
     s.k_blocks = cdiv(g.m, kTileK);
   } else {
-    s.tiles_m = cdiv(g.m, kTileM);
-    s.tiles_n = cdiv(g.m, bn);
+    s.tiles_n = cdiv(g.m, kTileN);  // == tiles_m
     s.tiles_per_mat = 0;
-    for (int tm = 0; tm < s.tiles_m; ++tm) s.tiles_per_mat += s.tiles_n - (tm * kTileM) / bn;
+    for (int p = 0; p < s.tiles_m; ++p) s.tiles_per_mat += s.tiles_n - p;
     s.k_blocks = cdiv(stage == kStageGram ? g.n : g.m, kTileK);
   }
   return s;
@@ -263,21 +281,20 @@ double stage_flops(const GPlan& g, int stage) {
 
 // Builds the launch block of one stage for a chunk of tensor-core groups.
 // `cur` selects X0 (0) or X1 (1) as this round's X.
-muon_status build_gemm(GemmLaunch& L, const std::vector<GPlan*>& chunk, int stage, int bn,
-                       int cur, bool first_round, bool last_round, int mode, const Scalars& sc,
-                       uint8_t* ws) {
+muon_status build_gemm(GemmLaunch& L, const std::vector<GPlan*>& chunk, int stage,
+                       int cur, bool first_round, const Scalars& sc, uint8_t* ws) {
   std::memset(&L, 0, sizeof(L));
   // heaviest problems first: their tiles are handed out first
   std::vector<GPlan*> order(chunk);
   std::stable_sort(order.begin(), order.end(), [&](GPlan* x, GPlan* y) {
-    const StageShape sx = stage_shape(*x, stage, bn), sy = stage_shape(*y, stage, bn);
+    const StageShape sx = stage_shape(*x, stage), sy = stage_shape(*y, stage);
     return sx.k_blocks > sy.k_blocks;
   });
   int tiles = 0;
   for (size_t i = 0; i < order.size(); ++i) {
     const GPlan& g = *order[i];
     GemmProblem& P = L.prob[i];
-    const StageShape ss = stage_shape(g, stage, bn);
+    const StageShape ss = stage_shape(g, stage);
     P.batch = g.batch;
     P.m = g.m;
     P.n = g.n;
@@ -291,32 +308,25 @@ muon_status build_gemm(GemmLaunch& L, const std::vector<GPlan*>& chunk, int stag
     tiles += ss.tiles_per_mat * g.batch;
     const uint8_t* xc = ws + (cur ? g.x1 : g.x0);
     uint8_t* xn = ws + (cur ? g.x0 : g.x1);
-    P.x_cur = reinterpret_cast<const __nv_bfloat16*>(xc);
-    P.x_next = reinterpret_cast<__nv_bfloat16*>(xn);
     P.a_mat = reinterpret_cast<const __nv_bfloat16*>(ws + g.am);
-    P.sym_out = reinterpret_cast<__nv_bfloat16*>(ws + (stage == kStageGram ? g.am : g.bm));
     P.parts = reinterpret_cast<const float*>(ws + g.parts);
     P.nparts = g.nparts;
     P.first_round = first_round ? 1 : 0;
-    P.out_mode = !last_round ? kOutX : (mode == kPrologueNsOnly ? kOutBf16 : kOutParam);
-    P.tall = g.tall ? 1 : 0;
-    P.param = g.p;
-    P.out = g.out;
-    const float scale = g.lr_scale > 0.f ? g.lr_scale
-                                          : static_cast<float>(std::sqrt(std::max(
-                                                1.0, static_cast<double>(g.r) / g.c)));
-    P.lr_eff = sc.lr * scale;
-    P.decay = 1.0f - sc.lr * sc.wd;
     bool ok = true;
-    if (stage == kStageGram) {
-      ok = make_tmap(&L.tm_a[i], xc, g.n, g.m, g.batch, g.ldx, kTileM) &&
-           make_tmap(&L.tm_b[i], xc, g.n, g.m, g.batch, g.ldx, bn);
-    } else if (stage == kStagePoly) {
-      ok = make_tmap(&L.tm_a[i], ws + g.am, g.m, g.m, g.batch, g.lda, kTileM) &&
-           make_tmap(&L.tm_b[i], ws + g.am, g.m, g.m, g.batch, g.lda, bn);
-    } else {
-      ok = make_tmap(&L.tm_a[i], ws + g.bm, g.m, g.m, g.batch, g.lda, kTileM) &&
-           make_tmap(&L.tm_b[i], xc, g.n, g.m, g.batch, g.ldx, 64);
+    if (stage == kStageGram) {          // A = s^2 X X^T
+      ok = operand_tmap(&L.tm_a[i], xc, g.n, g.m, g.batch, g.ldx, kTileM) &&
+           operand_tmap(&L.tm_b[i], xc, g.n, g.m, g.batch, g.ldx, kTileM) &&
+           output_tmap(&L.tm_out[i], ws + g.am, g.m, g.m, g.batch, g.lda, true) &&
+           output_tmap(&L.tm_mir[i], ws + g.am, g.m, g.m, g.batch, g.lda, false);
+    } else if (stage == kStagePoly) {   // B' = a I + b A + c A A
+      ok = operand_tmap(&L.tm_a[i], ws + g.am, g.m, g.m, g.batch, g.lda, kTileM) &&
+           operand_tmap(&L.tm_b[i], ws + g.am, g.m, g.m, g.batch, g.lda, kTileM) &&
+           output_tmap(&L.tm_out[i], ws + g.bm, g.m, g.m, g.batch, g.lda, true) &&
+           output_tmap(&L.tm_mir[i], ws + g.bm, g.m, g.m, g.batch, g.lda, false);
+    } else {                            // X' = s B' X
+      ok = operand_tmap(&L.tm_a[i], ws + g.bm, g.m, g.m, g.batch, g.lda, kTileM) &&
+           operand_tmap(&L.tm_b[i], xc, g.n, g.m, g.batch, g.ldx, 64) &&
+           output_tmap(&L.tm_out[i], xn, g.n, g.m, g.batch, g.ldx, true);
     }
     if (!ok) return MUON_ERR_CUDA;
   }
@@ -448,35 +458,61 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
   for (size_t c0 = 0; c0 < big.size(); c0 += kMaxProblems) {
     std::vector<GPlan*> chunk(big.begin() + c0,
                               big.begin() + std::min(big.size(), c0 + kMaxProblems));
-    int max_n = 0;
-    for (GPlan* g : chunk) max_n = std::max(max_n, g->n);
-    const int bn_upd = max_n > 128 ? 256 : 128;
     for (int it = 0; it < sc.steps; ++it) {
       const int cur = it & 1;
-      const bool first = (it == 0), last = (it == sc.steps - 1);
+      const bool first = (it == 0);
       const int stages[3] = {kStageGram, kStagePoly, kStageUpdate};
       for (int stage : stages) {
-        const int bn = (stage == kStageUpdate) ? bn_upd : 128;
         GemmLaunch L;
-        s = build_gemm(L, chunk, stage, bn, cur, first, last, sc.mode, sc, ws);
+        s = build_gemm(L, chunk, stage, cur, first, sc, ws);
         if (s != MUON_OK) return s;
         if (L.total_tiles == 0) continue;
-        double flops = 0, bytes = 0;
-        for (GPlan* g : chunk) {
-          flops += stage_flops(*g, stage);
-          if (stage == kStageUpdate && last && sc.mode != kPrologueNsOnly)
-            bytes += static_cast<double>(g->batch) * g->m * g->n * 8.0;
-        }
+        double flops = 0;
+        for (GPlan* g : chunk) flops += stage_flops(*g, stage);
         const int kind = stage == kStageGram   ? MUON_K_GRAM
                          : stage == kStagePoly ? MUON_K_POLY
-                         : last                ? MUON_K_UPDATE_APPLY
                                                : MUON_K_UPDATE;
-        const int grid = std::min(L.total_tiles, sms);
-        const cudaError_t e = tracked_launch(st, {kind, it, flops, bytes},
-                                             [&] { return launch_gemm(L, stage, bn, grid, st); });
+        const cudaError_t e =
+            tracked_launch(st, {kind, it, flops, 0.0},
+                           [&] { return launch_gemm(L, stage, L.total_tiles, sms, st); });
         if (e != cudaSuccess) return MUON_ERR_CUDA;
       }
     }
+  }
+
+  // -- apply: p <- (1 - lr wd) p - lr rescale O (or O as bf16), one grouped launch;
+  //    after round `steps` the result sits in X1 if steps is odd, else in X0
+  for (size_t c0 = 0; c0 < big.size(); c0 += kMaxPrologueGroups) {
+    ApplyLaunch al;
+    std::memset(&al, 0, sizeof(al));
+    double bytes = 0;
+    int blocks = 0;
+    for (size_t k = c0; k < std::min(big.size(), c0 + kMaxPrologueGroups); ++k) {
+      const GPlan& g = *big[k];
+      ApplyGroup& ag = al.grp[al.n_groups++];
+      ag.o = reinterpret_cast<const __nv_bfloat16*>(ws + ((sc.steps & 1) ? g.x1 : g.x0));
+      ag.param = g.p;
+      ag.out = g.out;
+      ag.batch = g.batch;
+      ag.r = g.r;
+      ag.c = g.c;
+      ag.ldx = g.ldx;
+      ag.nparts = g.nparts;
+      ag.block_begin = blocks;
+      const float scale = g.lr_scale > 0.f ? g.lr_scale
+                                            : static_cast<float>(std::sqrt(std::max(
+                                                  1.0, static_cast<double>(g.r) / g.c)));
+      ag.lr_eff = sc.lr * scale;
+      ag.decay = 1.0f - sc.lr * sc.wd;
+      blocks += g.batch * g.nparts;
+      bytes += static_cast<double>(g.batch) * g.r * g.c *
+               (sc.mode == kPrologueNsOnly ? 4.0 : 10.0);
+    }
+    al.total_blocks = blocks;
+    const bool to_param = sc.mode != kPrologueNsOnly;
+    const cudaError_t e = tracked_launch(st, {MUON_K_APPLY, -1, 0.0, bytes},
+                                         [&] { return launch_apply(al, to_param, st); });
+    if (e != cudaSuccess) return MUON_ERR_CUDA;
   }
   return MUON_OK;
 }

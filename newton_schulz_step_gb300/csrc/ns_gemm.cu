@@ -3,49 +3,65 @@
 // section 核心思想: A = X X^T; B = b A + c A A; X = a X + B X):
 //
 //   Gram    A = s^2 X X^T      (s = 1/(||u||_F + eps) on the first round, else 1)
-//   Poly    B = b A + c A A
-//   Update  X' = s (a X + B X), or on the last round the parameter write
-//           p <- (1 - lr wd) p - lr rescale X'   (or a bf16 copy of X')
+//   Poly    B' = a I + b A + c A A
+//   Update  X' = s B' X  (= s (a X + B X))
+//
+// (The parameter write that follows the last round is the elementwise apply
+// kernel in prologue.cu.)
+// Folding a I into the polynomial's output makes the update a plain GEMM with
+// no X operand in its epilogue; rounding a + B_ii to bf16 once was checked to
+// cost no accuracy against adding a X in fp32.
 //
 // X is m x n (m <= n) bf16, row-major with padded leading dimension; A and B
 // are m x m bf16.  A and B are symmetric, so Gram and Poly compute only the
-// tiles on or above the diagonal and store every entry once directly and once
-// mirrored.  For A A the second operand A[k][j] = A[j][k] is then read K-major
-// like the first; only the Update's X operand (contraction over X's rows) is
-// MN-major.
+// tiles that hold entries on or above the diagonal and store every such entry
+// once directly and once mirrored.  For A A the second operand A[k][j] =
+// A[j][k] is then read K-major like the first; only the Update's X operand
+// (contraction over X's rows) is MN-major.
 //
-// Kernel shape: persistent, one CTA per SM, 192 threads:
+// Kernel shape: persistent clusters of two CTAs, one CTA per SM, 192 threads:
 //   warp 0      TMA producer (one lane) into a ring of swizzled smem stages
 //   warp 1      TMEM allocator and tcgen05.mma issuer (one lane)
-//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator, fp32 math,
-//               global stores
-// The accumulator is double-buffered in TMEM so the epilogue of one tile
-// overlaps the MMAs of the next.  Tiles of all problems of the launch form one
-// linear list, walked with a stride of gridDim.x.
+//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator, fp32 math, 32 x 32
+//               blocks staged in shared memory and written by TMA bulk stores
+//               (Gram and Poly also store each block's mirror the same way)
+// Each CTA computes a 128 x 256 tile; the two CTAs of a cluster take tile rows
+// 2p and 2p+1 of the same tile column, so they need the same B operand: each
+// loads half of it and multicasts that half to both, halving the B traffic
+// out of L2.  With 256-wide tile columns the two rows of a pair also have the
+// same set of upper-triangle tiles, so symmetric stages pair up exactly.  A
+// stage slot is reused only after both CTAs' MMAs have read it (each MMA warp
+// commits to the empty barriers of both CTAs).  The accumulator is double
+// buffered in TMEM so the epilogue of one tile overlaps the MMAs of the next.
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace muon {
 
-template <int BN>
 struct GemmCfg {
-  static constexpr int kStages = (BN == 256) ? 4 : 6;
-  static constexpr int kABytes = kTileM * kTileK * 2;  // 16 KB: 128 rows x 128 B
-  static constexpr int kBBytes = BN * kTileK * 2;      // BN rows (or BN/64 slabs) x 128 B
-  static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kBN = 256;
+  static constexpr int kStages = 4;
+  static constexpr int kABytes = kTileM * kTileK * 2;    // 16 KB: 128 rows x 128 B
+  static constexpr int kBBytes = kBN * kTileK * 2;       // 32 KB
+  static constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
+  static constexpr int kTmemCols = 2 * kBN;              // two 128 x 256 fp32 accumulators
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kSlotBytes = 4096;                     // per warp, per slot
+  static constexpr int kStagingBytes = kEpiWarps * 2 * kSlotBytes;
   static constexpr int kBarBytes = 256;
-  static constexpr int kSmem = kStages * kStageBytes + kBarBytes + 1024;
+  static constexpr int kSmem = kStages * kStageBytes + kStagingBytes + kBarBytes + 1024;
 };
+constexpr uint16_t kPairMask = 0x3;
 
 struct Tile {
-  int prob, mat, tm, tn;
+  int prob, mat, tm, tn;  // tm: this CTA's tile row (2 * pair row + cluster rank)
 };
 
-// Linear tile index -> (problem, matrix, tile row, tile col).  Symmetric
-// stages enumerate, per tile row tm, the tile columns tn >= floor(tm*128/BN).
-template <int STAGE, int BN>
-__device__ __forceinline__ Tile decode_tile(const GemmLaunch& L, int t) {
+// Linear pair-tile index -> (problem, matrix, tile row of this CTA, tile col).
+// Symmetric stages enumerate, per pair row p, the tile columns tn >= p.
+template <int STAGE>
+__device__ __forceinline__ Tile decode_tile(const GemmLaunch& L, int t, int rank) {
   int p = 0;
 #pragma unroll 1
   while (p + 1 < L.n_prob && t >= L.prob[p + 1].tile_begin) ++p;
@@ -55,24 +71,24 @@ __device__ __forceinline__ Tile decode_tile(const GemmLaunch& L, int t) {
   r.prob = p;
   r.mat = local / P.tiles_per_mat;
   int w = local - r.mat * P.tiles_per_mat;
-  if (STAGE == kStageUpdate) {
-    r.tm = w / P.tiles_n;
-    r.tn = w - r.tm * P.tiles_n;
+  int tp = P.tiles_m;  // out of range unless found (no stores then)
+  if (STAGE >= kStageUpdate) {
+    tp = w / P.tiles_n;
+    r.tn = w - tp * P.tiles_n;
   } else {
-    r.tm = P.tiles_m;  // out of range unless found (no stores then)
     r.tn = 0;
 #pragma unroll 1
-    for (int tm = 0; tm < P.tiles_m; ++tm) {
-      const int first = (tm * kTileM) / BN;
-      const int cnt = P.tiles_n - first;
+    for (int q = 0; q < P.tiles_m; ++q) {
+      const int cnt = P.tiles_n - q;
       if (w < cnt) {
-        r.tm = tm;
-        r.tn = first + w;
+        tp = q;
+        r.tn = q + w;
         break;
       }
       w -= cnt;
     }
   }
+  r.tm = 2 * tp + rank;
   return r;
 }
 
@@ -82,11 +98,14 @@ __device__ __forceinline__ void record_failure(const GemmLaunch& L, volatile int
   atomicOr(L.status, bit);
 }
 
+__device__ __forceinline__ int first_tile() { return blockIdx.x >> 1; }
+__device__ __forceinline__ int tile_stride() { return gridDim.x >> 1; }
+
 // ------------------------------------------------------------ producer
-template <int STAGE, int BN>
+template <int STAGE>
 __device__ void run_producer(const GemmLaunch& L, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                             volatile int* abort_flag) {
-  using C = GemmCfg<BN>;
+                             volatile int* abort_flag, int rank) {
+  using C = GemmCfg;
   for (int p = 0; p < L.n_prob; ++p) {
     ptx::prefetch_tmap(&L.tm_a[p]);
     ptx::prefetch_tmap(&L.tm_b[p]);
@@ -95,12 +114,13 @@ __device__ void run_producer(const GemmLaunch& L, uint8_t* smem, uint64_t* full,
   uint32_t phase = 0;
   uint32_t armed = 0, armed_parity = 0;
   bool ok = true;
-  for (int t = blockIdx.x; ok && t < L.total_tiles; t += gridDim.x) {
-    const Tile tl = decode_tile<STAGE, BN>(L, t);
+  for (int t = first_tile(); ok && t < L.total_tiles; t += tile_stride()) {
+    const Tile tl = decode_tile<STAGE>(L, t, rank);
     const GemmProblem& P = L.prob[tl.prob];
     const CUtensorMap* ta = &L.tm_a[tl.prob];
     const CUtensorMap* tb = &L.tm_b[tl.prob];
     for (int kb = 0; kb < P.k_blocks; ++kb) {
+      // both CTAs' MMAs must be done with this slot: the peer's half lands here too
       if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
         record_failure(L, abort_flag, kErrTimeoutProducer);
         ok = false;
@@ -109,17 +129,23 @@ __device__ void run_producer(const GemmLaunch& L, uint8_t* smem, uint64_t* full,
       uint8_t* sa = smem + stage * C::kStageBytes;
       uint8_t* sb = sa + C::kABytes;
       ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-      // operand A: 128 rows (tile row tm) x 64 k-columns
+      // operand A: this CTA's 128 rows x 64 k-columns
       ptx::tma_load_3d(sa, ta, kb * kTileK, tl.tm * kTileM, tl.mat, &full[stage]);
-      if (STAGE == kStageUpdate) {
-        // operand B = X[k][j], MN-major: BN/64 slabs of 64 columns x 64 k-rows
+      if (STAGE >= kStageUpdate) {
+        // operand B = X[k][j], MN-major: 4 slabs of 64 columns x 64 k-rows; this
+        // CTA loads slabs 2*rank, 2*rank+1 for both CTAs
 #pragma unroll
-        for (int q = 0; q < BN / 64; ++q)
-          ptx::tma_load_3d(sb + q * (64 * kTileK * 2), tb, tl.tn * BN + q * 64, kb * kTileK,
-                           tl.mat, &full[stage]);
+        for (int q = 0; q < 2; ++q) {
+          const int slab = 2 * rank + q;
+          ptx::tma_load_3d_multicast(sb + slab * (64 * kTileK * 2), tb, tl.tn * C::kBN + slab * 64,
+                                     kb * kTileK, tl.mat, &full[stage], kPairMask);
+        }
       } else {
-        // operand B: BN rows (tile col tn) x 64 k-columns, K-major
-        ptx::tma_load_3d(sb, tb, kb * kTileK, tl.tn * BN, tl.mat, &full[stage]);
+        // operand B: 256 rows (tile col tn) x 64 k-columns, K-major; this CTA
+        // loads rows 128*rank .. +127 for both CTAs
+        ptx::tma_load_3d_multicast(sb + rank * C::kABytes, tb, kb * kTileK,
+                                   tl.tn * C::kBN + rank * kTileM, tl.mat, &full[stage],
+                                   kPairMask);
       }
       armed |= 1u << stage;
       armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -129,35 +155,41 @@ __device__ void run_producer(const GemmLaunch& L, uint8_t* smem, uint64_t* full,
       }
     }
   }
-  // Every armed stage's copies have landed before the CTA may exit.
-  for (int s = 0; s < C::kStages; ++s)
-    if (armed & (1u << s))
-      if (!ptx::mbar_wait(&full[s], (armed_parity >> s) & 1u, nullptr))
+  // Before exit: every armed stage's copies (own and the peer's) have landed,
+  // and both CTAs' MMAs have released it, so no multicast copy or remote
+  // commit arrival can still be on its way to this CTA.
+  for (int s = 0; s < C::kStages; ++s) {
+    if (armed & (1u << s)) {
+      const uint32_t par = (armed_parity >> s) & 1u;
+      if (!ptx::mbar_wait(&full[s], par, nullptr)) record_failure(L, abort_flag, kErrTimeoutDrain);
+      if (!ptx::mbar_wait(&empty[s], par, nullptr))
         record_failure(L, abort_flag, kErrTimeoutDrain);
+    }
+  }
 }
 
 // ------------------------------------------------------------ MMA issuer
-template <int STAGE, int BN>
+template <int STAGE>
 __device__ void run_mma(const GemmLaunch& L, uint8_t* smem, uint64_t* full, uint64_t* empty,
                         uint64_t* acc_full, uint64_t* acc_empty, uint64_t* drain,
-                        uint32_t tmem_base, volatile int* abort_flag) {
-  using C = GemmCfg<BN>;
-  constexpr bool kBmn = (STAGE == kStageUpdate);
-  constexpr uint32_t kIdesc = ptx::idesc_bf16_m128(BN, kBmn);
+                        uint32_t tmem_base, volatile int* abort_flag, int rank) {
+  using C = GemmCfg;
+  constexpr bool kBmn = (STAGE >= kStageUpdate);
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_m128(C::kBN, kBmn);
   int stage = 0;
   uint32_t phase = 0;
   int acc = 0;
   uint32_t acc_phase = 0;
   bool ok = true;
-  for (int t = blockIdx.x; ok && t < L.total_tiles; t += gridDim.x) {
-    const Tile tl = decode_tile<STAGE, BN>(L, t);
+  for (int t = first_tile(); ok && t < L.total_tiles; t += tile_stride()) {
+    const Tile tl = decode_tile<STAGE>(L, t, rank);
     const int kblocks = L.prob[tl.prob].k_blocks;
     if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
       record_failure(L, abort_flag, kErrTimeoutMma);
       break;
     }
     ptx::tc_fence_after();
-    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::kBN);
     for (int kb = 0; kb < kblocks; ++kb) {
       if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) {
         record_failure(L, abort_flag, kErrTimeoutMma);
@@ -177,7 +209,8 @@ __device__ void run_mma(const GemmLaunch& L, uint8_t* smem, uint64_t* full, uint
                                  : ptx::smem_desc_sw128(sb + k * 32, 16, 1024);
         ptx::mma_bf16(d_tmem, da, db, kIdesc, (kb | k) != 0 ? 1u : 0u);
       }
-      ptx::mma_commit(&empty[stage]);  // frees the stage once these MMAs finish
+      // frees the slot in both CTAs once these MMAs have read it
+      ptx::mma_commit_multicast(&empty[stage], kPairMask);
       if (++stage == C::kStages) {
         stage = 0;
         phase ^= 1u;
@@ -209,6 +242,11 @@ __device__ __forceinline__ float inv_fro_norm(const float* parts, int nparts, fl
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b2);
+}
+
 // 32 consecutive bf16 of a row (zero past `valid`), kept packed.
 __device__ __forceinline__ void load_row32(const __nv_bfloat16* src, int valid,
                                            uint32_t (&w)[16]) {
@@ -233,181 +271,69 @@ __device__ __forceinline__ void load_row32(const __nv_bfloat16* src, int valid,
   }
 }
 
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, int valid, const float (&f)[32]) {
-  if (valid >= 32) {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t ws[4];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(f[q * 8 + 2 * h], f[q * 8 + 2 * h + 1]);
-        ws[h] = *reinterpret_cast<uint32_t*>(&b2);
-      }
-      d4[q] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
-    }
-  } else {
-#pragma unroll
-    for (int t = 0; t < 32; ++t)
-      if (t < valid) dst[t] = __float2bfloat16_rn(f[t]);
-  }
+// Output staging.  Each epilogue warp owns two 4 KB slots used in turn:
+//   [0, 2 KB)  the warp's 32 x 32 block of the output, bf16, 64-byte rows with
+//              the 64-byte swizzle TMA expects (16-byte unit u of row r sits
+//              at unit u ^ ((r >> 1) & 3)), written with 16-byte stores;
+//   [2, 4 KB)  the mirrored block (entry (i, j) at row j, column i), bf16, no
+//              swizzle: lanes hold consecutive i, so its stores are
+//              conflict-free.
+// Both are stored to global memory by one TMA bulk store each.
+__device__ __forceinline__ uint32_t sw64(int r, int c) {
+  return static_cast<uint32_t>(r * 64 + ((((c >> 3) ^ (r >> 1)) & 3) << 4) + (c & 7) * 2);
 }
 
-// Parameter values the apply epilogue of chunk (i, j0) overwrites.  Not tall:
-// p[i][j0..j0+31] of a [m, n] matrix; tall: p[j0+t][i] of an [n, m] matrix
-// (lanes hold consecutive i, so each access is coalesced across the warp).
-__device__ __forceinline__ void load_params32(const GemmProblem& P, int mat, int i, int j0,
-                                              float (&pv)[32]) {
-  const int m = P.m, n = P.n;
-  const size_t moff = static_cast<size_t>(mat) * m * n;
-  const int valid = n - j0;
-  if (!P.tall) {
-    const float* pr = P.param + moff + static_cast<size_t>(i) * n + j0;
-    if (valid >= 32 && (n & 3) == 0) {
-      const float4* p4 = reinterpret_cast<const float4*>(pr);
+__device__ __forceinline__ void stage_row_sw64(uint8_t* blk, int r, const float (&v)[32]) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 w = p4[q];
-        pv[4 * q + 0] = w.x;
-        pv[4 * q + 1] = w.y;
-        pv[4 * q + 2] = w.z;
-        pv[4 * q + 3] = w.w;
-      }
-    } else {
-#pragma unroll
-      for (int t = 0; t < 32; ++t) pv[t] = (t < valid) ? pr[t] : 0.f;
-    }
-  } else {
-    const float* pc = P.param + moff + static_cast<size_t>(j0) * m + i;
-#pragma unroll
-    for (int t = 0; t < 32; ++t) pv[t] = (t < valid) ? pc[static_cast<size_t>(t) * m] : 0.f;
-  }
-}
-
-// Final output of chunk (i, j0) in the input's orientation: the parameter
-// write p <- decay p - lr_eff x (kOutParam) or a bf16 copy of x (kOutBf16).
-__device__ __forceinline__ void store_output32(const GemmProblem& P, int mat, int i, int j0,
-                                               const float (&x)[32], const float (&pv)[32]) {
-  const int m = P.m, n = P.n;
-  const size_t moff = static_cast<size_t>(mat) * m * n;
-  const int valid = n - j0;
-  float o[32];
-  if (P.out_mode == kOutParam) {
-#pragma unroll
-    for (int t = 0; t < 32; ++t) o[t] = fmaf(-P.lr_eff, x[t], P.decay * pv[t]);
-  } else {
-#pragma unroll
-    for (int t = 0; t < 32; ++t) o[t] = x[t];
-  }
-  if (!P.tall) {
-    const size_t base = moff + static_cast<size_t>(i) * n + j0;
-    if (P.out_mode == kOutParam) {
-      float* pr = P.param + base;
-      if (valid >= 32 && (n & 3) == 0) {
-        float4* p4 = reinterpret_cast<float4*>(pr);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          p4[q] = make_float4(o[4 * q + 0], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-      } else {
-#pragma unroll
-        for (int t = 0; t < 32; ++t)
-          if (t < valid) pr[t] = o[t];
-      }
-    } else {
-      __nv_bfloat16* orow = P.out + base;
-      if (valid >= 32 && (n & 7) == 0) {
-        store_row32(orow, 32, o);
-      } else {
-#pragma unroll
-        for (int t = 0; t < 32; ++t)
-          if (t < valid) orow[t] = __float2bfloat16_rn(o[t]);
-      }
-    }
-  } else {
-    const size_t base = moff + static_cast<size_t>(j0) * m + i;
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      if (t < valid) {
-        if (P.out_mode == kOutParam)
-          P.param[base + static_cast<size_t>(t) * m] = o[t];
-        else
-          P.out[base + static_cast<size_t>(t) * m] = __float2bfloat16_rn(o[t]);
-      }
-    }
-  }
-}
-
-// Gram / Poly chunk: row i, columns j0..j0+31 of the symmetric output; stores
-// the entries on/above the diagonal directly and those above it mirrored.
-template <int STAGE>
-__device__ __forceinline__ void epilogue_sym_chunk(const GemmLaunch& L, const GemmProblem& P,
-                                                   int mat, int i, int j0, float scale,
-                                                   const uint32_t (&v)[32],
-                                                   const uint32_t (&av)[16]) {
-  const int m = P.m, ld = P.lda;
-  __nv_bfloat16* out = P.sym_out + static_cast<size_t>(mat) * m * ld;
-  float val[32];
-  if (STAGE == kStageGram) {
-#pragma unroll
-    for (int t = 0; t < 32; ++t) val[t] = __uint_as_float(v[t]) * scale;
-  } else {
-#pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      val[2 * t] = fmaf(L.c, __uint_as_float(v[2 * t]), L.b * bf_lo(av[t]));
-      val[2 * t + 1] = fmaf(L.c, __uint_as_float(v[2 * t + 1]), L.b * bf_hi(av[t]));
-    }
-  }
-  __nv_bfloat16* orow = out + static_cast<size_t>(i) * ld + j0;
-  if (j0 + 32 <= m && j0 >= i) {
-    store_row32(orow, 32, val);
-  } else {
-#pragma unroll
-    for (int t = 0; t < 32; ++t)
-      if (j0 + t >= i && j0 + t < m) orow[t] = __float2bfloat16_rn(val[t]);
-  }
-#pragma unroll
-  for (int t = 0; t < 32; ++t) {
-    const int j = j0 + t;
-    if (j > i && j < m) out[static_cast<size_t>(j) * ld + i] = __float2bfloat16_rn(val[t]);
+  for (int q = 0; q < 4; ++q) {
+    const uint4 w = make_uint4(pack_bf2(v[8 * q + 0], v[8 * q + 1]),
+                               pack_bf2(v[8 * q + 2], v[8 * q + 3]),
+                               pack_bf2(v[8 * q + 4], v[8 * q + 5]),
+                               pack_bf2(v[8 * q + 6], v[8 * q + 7]));
+    *reinterpret_cast<uint4*>(blk + sw64(r, 8 * q)) = w;
   }
 }
 
 // ------------------------------------------------------------ epilogue warps
-// Operands a chunk needs besides the accumulator are loaded one chunk ahead
-// (the first chunk before waiting for the accumulator), so their latency
-// overlaps the TMEM load and the previous chunk's math and stores.
-template <int STAGE, int BN>
+// Warp w (2..5) owns TMEM lanes 32*(w&3).. (32 rows of the 128-row tile) and
+// walks the tile's 256 columns in 8 chunks of 32.
+template <int STAGE>
 __device__ void run_epilogue(const GemmLaunch& L, uint64_t* acc_full, uint64_t* acc_empty,
-                             uint32_t tmem_base, volatile int* abort_flag, int warp, int lane) {
-  const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-  const int row = quarter * 32 + lane;
+                             uint32_t tmem_base, uint8_t* staging, volatile int* abort_flag,
+                             int warp, int lane, int rank) {
+  using C = GemmCfg;
+  constexpr int kChunks = C::kBN / 32;
+  constexpr bool kSym = STAGE <= kStagePoly;
+  // the Poly operand ring needs static indices: full unroll
+  const int quarter = warp & 3;
+  uint8_t* my_slots = staging + quarter * 2 * C::kSlotBytes;
   int acc = 0;
   uint32_t acc_phase = 0;
-  for (int t = blockIdx.x; t < L.total_tiles; t += gridDim.x) {
+  int slot = 0;
+  for (int t = first_tile(); t < L.total_tiles; t += tile_stride()) {
     __syncwarp();
-    const Tile tl = decode_tile<STAGE, BN>(L, t);
+    const Tile tl = decode_tile<STAGE>(L, t, rank);
     const GemmProblem& P = L.prob[tl.prob];
+    const CUtensorMap* tm_out = &L.tm_out[tl.prob];
+    const CUtensorMap* tm_mir = &L.tm_mir[tl.prob];
     float s = 1.f;
     if (STAGE != kStagePoly && P.first_round)
       s = inv_fro_norm(P.parts + static_cast<size_t>(tl.mat) * P.nparts, P.nparts, L.eps, lane);
-    const int i = tl.tm * kTileM + row;
-    const bool row_ok = i < P.m;
-    const int ncols = (STAGE == kStageUpdate) ? P.n : P.m;
-    const bool need_e = (STAGE != kStageGram);
-    const bool need_p = (STAGE == kStageUpdate) && P.out_mode == kOutParam;
-    const size_t ld = (STAGE == kStageUpdate) ? P.ldx : P.lda;
-    const __nv_bfloat16* esrc =
-        (STAGE == kStageUpdate ? P.x_cur : P.a_mat) +
-        static_cast<size_t>(tl.mat) * P.m * ld + static_cast<size_t>(row_ok ? i : 0) * ld;
+    const int i0 = tl.tm * kTileM + quarter * 32;  // first row of this warp
+    const int i = i0 + lane;
+    const bool rows_live = i0 < P.m;                // warp-uniform
+    const int ncols = kSym ? P.m : P.n;
+    const int jt = tl.tn * C::kBN;
 
-    uint32_t e_cur[16], e_nxt[16];
-    float p_cur[32], p_nxt[32];
-    {
-      const int j0 = tl.tn * BN;
-      if (row_ok && j0 < ncols) {
-        if (need_e) load_row32(esrc + j0, ncols - j0, e_cur);
-        if (need_p) load_params32(P, tl.mat, i, j0, p_cur);
-      }
+    // Poly: the b A term, loaded two chunks ahead (row i of A, 64 bytes per chunk)
+    uint32_t e[3][16];
+    const __nv_bfloat16* arow =
+        P.a_mat + static_cast<size_t>(tl.mat) * P.m * P.lda +
+        static_cast<size_t>(i < P.m ? i : 0) * P.lda;
+    if (STAGE == kStagePoly && i < P.m) {
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch)
+        if (jt + 32 * ch < ncols) load_row32(arow + jt + 32 * ch, ncols - jt - 32 * ch, e[ch]);
     }
     const bool got = ptx::mbar_wait(&acc_full[acc], acc_phase, abort_flag);
     __syncwarp();
@@ -417,43 +343,76 @@ __device__ void run_epilogue(const GemmLaunch& L, uint64_t* acc_full, uint64_t* 
     }
     ptx::tc_fence_after();
     const uint32_t tbase =
-        tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
-#pragma unroll 1
-    for (int ch = 0; ch < BN / 32; ++ch) {
-      const int j0 = tl.tn * BN + ch * 32;
+        tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * C::kBN);
+#pragma unroll
+    for (int ch = 0; ch < kChunks; ++ch) {
+      const int j0 = jt + ch * 32;
       if (j0 >= ncols) break;  // warp-uniform
-      const int jn = j0 + 32;
-      if (row_ok && ch + 1 < BN / 32 && jn < ncols) {
-        if (need_e) load_row32(esrc + jn, ncols - jn, e_nxt);
-        if (need_p) load_params32(P, tl.mat, i, jn, p_nxt);
+      if constexpr (STAGE == kStagePoly) {
+        if (i < P.m && ch + 2 < kChunks && j0 + 64 < ncols)
+          load_row32(arow + j0 + 64, ncols - j0 - 64, e[(ch + 2) % 3]);
       }
       __syncwarp();
       uint32_t v[32];
       ptx::tmem_ld32(tbase + static_cast<uint32_t>(ch * 32), v);
       ptx::tmem_ld_wait();
-      if (row_ok) {
-        if (STAGE == kStageUpdate) {
-          float x[32];
+      // symmetric stages: blocks wholly below the diagonal belong to the mirror
+      // of another block and are skipped
+      const bool live = rows_live && !(kSym && j0 < i0);
+      if (live) {
+        float val[32];
+        if constexpr (STAGE == kStageGram) {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) val[q] = __uint_as_float(v[q]) * (s * s);
+        } else if constexpr (STAGE == kStagePoly) {
+          const uint32_t(&ev)[16] = e[ch % 3];
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
-            x[2 * q] = s * fmaf(L.a, bf_lo(e_cur[q]), __uint_as_float(v[2 * q]));
-            x[2 * q + 1] = s * fmaf(L.a, bf_hi(e_cur[q]), __uint_as_float(v[2 * q + 1]));
+            val[2 * q] = fmaf(L.c, __uint_as_float(v[2 * q]), L.b * bf_lo(ev[q]));
+            val[2 * q + 1] = fmaf(L.c, __uint_as_float(v[2 * q + 1]), L.b * bf_hi(ev[q]));
           }
-          if (P.out_mode == kOutX)
-            store_row32(P.x_next + static_cast<size_t>(tl.mat) * P.m * P.ldx +
-                            static_cast<size_t>(i) * P.ldx + j0,
-                        ncols - j0, x);
-          else
-            store_output32(P, tl.mat, i, j0, x, p_cur);
+          // B' = a I + b A + c A A: the update then needs no a X term
+          if (j0 == i0) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) val[q] += (q == lane) ? L.a : 0.f;
+          }
         } else {
-          epilogue_sym_chunk<STAGE>(L, P, tl.mat, i, j0, s * s, v, e_cur);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) val[q] = s * __uint_as_float(v[q]);
         }
-      }
+
+        // the slot's previous bulk store (two chunks ago) has read its data
+        if (lane == 0) ptx::bulk_wait_read<1>();
+        __syncwarp();
+        uint8_t* blk = my_slots + slot * C::kSlotBytes;
+        uint8_t* mir = blk + 2048;
+        const bool diag = kSym && j0 == i0;
+        if (!diag) {
+          stage_row_sw64(blk, lane, val);
+          if constexpr (kSym) {
 #pragma unroll
-      for (int q = 0; q < 16; ++q) e_cur[q] = e_nxt[q];
-      if (need_p) {
+            for (int q = 0; q < 32; ++q)
+              *reinterpret_cast<__nv_bfloat16*>(mir + q * 64 + lane * 2) =
+                  __float2bfloat16_rn(val[q]);
+          }
+        } else {
+          // diagonal block: assemble it whole; entry (r, c) with c >= r comes
+          // from thread r, its mirror (c, r) from the same value
 #pragma unroll
-        for (int q = 0; q < 32; ++q) p_cur[q] = p_nxt[q];
+          for (int q = 0; q < 32; ++q) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(val[q]);
+            if (q >= lane) *reinterpret_cast<__nv_bfloat16*>(blk + sw64(lane, q)) = h;
+            if (q > lane) *reinterpret_cast<__nv_bfloat16*>(blk + sw64(q, lane)) = h;
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_3d(tm_out, j0, i0, tl.mat, blk);
+          if (kSym && !diag) ptx::tma_store_3d(tm_mir, i0, j0, tl.mat, mir);
+          ptx::bulk_commit();
+        }
+        slot ^= 1;
       }
     }
     ptx::tc_fence_before();
@@ -464,16 +423,22 @@ __device__ void run_epilogue(const GemmLaunch& L, uint64_t* acc_full, uint64_t* 
       acc_phase ^= 1u;
     }
   }
+  // all bulk stores of this warp are complete before the CTA exits
+  if (lane == 0) ptx::bulk_wait<0>();
+  __syncwarp();
 }
 
 // ------------------------------------------------------------ kernel
-template <int STAGE, int BN>
-__global__ void __launch_bounds__(192, 1) ns_gemm_kernel(const __grid_constant__ GemmLaunch L) {
-  using C = GemmCfg<BN>;
+template <int STAGE>
+__global__ void __launch_bounds__(GemmCfg::kThreads, 1)
+    ns_gemm_kernel(const __grid_constant__ GemmLaunch L) {
+  using C = GemmCfg;
   extern __shared__ uint8_t smem_raw[];
+  // every CTA of the cluster gets the same aligned offsets (multicast targets)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  uint8_t* staging = smem + C::kStages * C::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + C::kStagingBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::kStages;
   uint64_t* acc_full = bars + 2 * C::kStages;
@@ -484,15 +449,16 @@ __global__ void __launch_bounds__(192, 1) ns_gemm_kernel(const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(ptx::cluster_ctarank());
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 1);
+      ptx::mbar_init(&empty[s], 2);  // one commit from each CTA's MMA warp
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&acc_full[s], 1);
-      ptx::mbar_init(&acc_empty[s], 4);
+      ptx::mbar_init(&acc_empty[s], C::kEpiWarps);
     }
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -502,23 +468,29 @@ __global__ void __launch_bounds__(192, 1) ns_gemm_kernel(const __grid_constant__
     ptx::tmem_alloc(tmem_slot, C::kTmemCols);
     ptx::tmem_relinquish();
   }
+  __syncwarp();
   ptx::tc_fence_before();
-  __syncthreads();
+  // both CTAs' barriers exist before either multicasts into the other
+  ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) run_producer<STAGE, BN>(L, smem, full, empty, abort_flag);
+    if (lane == 0) run_producer<STAGE>(L, smem, full, empty, abort_flag, rank);
   } else if (warp == 1) {
     if (lane == 0)
-      run_mma<STAGE, BN>(L, smem, full, empty, acc_full, acc_empty, drain, tmem_base, abort_flag);
+      run_mma<STAGE>(L, smem, full, empty, acc_full, acc_empty, drain, tmem_base, abort_flag,
+                     rank);
   } else {
-    run_epilogue<STAGE, BN>(L, acc_full, acc_empty, tmem_base, abort_flag, warp, lane);
+    run_epilogue<STAGE>(L, acc_full, acc_empty, tmem_base, staging, abort_flag, warp, lane,
+                        rank);
   }
 
   __syncwarp();
   ptx::tc_fence_before();
-  __syncthreads();
+  // neither CTA exits while the other may still write into its shared memory
+  // or arrive on its barriers
+  ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::kTmemCols);
@@ -526,37 +498,51 @@ __global__ void __launch_bounds__(192, 1) ns_gemm_kernel(const __grid_constant__
 }
 
 // ------------------------------------------------------------ launchers
-template <int STAGE, int BN>
-static cudaError_t launch_instance(const GemmLaunch& l, int grid, cudaStream_t s) {
-  constexpr int kSmem = GemmCfg<BN>::kSmem;
-  static int configured[64] = {0};
+template <int STAGE>
+static cudaError_t launch_instance(const GemmLaunch& l, int pair_tiles, int sms, cudaStream_t s) {
+  constexpr int kSmem = GemmCfg::kSmem;
+  static int max_clusters[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(ns_gemm_kernel<STAGE, BN>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(GemmCfg::kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // clusters that fit on the device at once (one CTA per SM), queried once
+  int n = dev < 64 ? max_clusters[dev] : 0;
+  if (n == 0) {
+    e = cudaFuncSetAttribute(ns_gemm_kernel<STAGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmem);
     if (e != cudaSuccess) return e;
-    configured[dev] = 1;
+    cfg.gridDim = dim3(2 * (sms / 2));
+    e = cudaOccupancyMaxActiveClusters(&n, ns_gemm_kernel<STAGE>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) n = 1;
+    if (dev < 64) max_clusters[dev] = n;
   }
-  ns_gemm_kernel<STAGE, BN><<<grid, 192, kSmem, s>>>(l);
-  return cudaGetLastError();
+  const int clusters = pair_tiles < n ? pair_tiles : n;
+  cfg.gridDim = dim3(2 * clusters);
+  return cudaLaunchKernelEx(&cfg, ns_gemm_kernel<STAGE>, l);
 }
 
-int gemm_smem_bytes(int stage, int bn) {
-  (void)stage;
-  return bn == 256 ? GemmCfg<256>::kSmem : GemmCfg<128>::kSmem;
-}
+int gemm_smem_bytes() { return GemmCfg::kSmem; }
 
-cudaError_t launch_gemm(const GemmLaunch& l, int stage, int bn, int grid, cudaStream_t s) {
+cudaError_t launch_gemm(const GemmLaunch& l, int stage, int pair_tiles, int sms, cudaStream_t s) {
   switch (stage) {
     case kStageGram:
-      return launch_instance<kStageGram, 128>(l, grid, s);
+      return launch_instance<kStageGram>(l, pair_tiles, sms, s);
     case kStagePoly:
-      return launch_instance<kStagePoly, 128>(l, grid, s);
+      return launch_instance<kStagePoly>(l, pair_tiles, sms, s);
     case kStageUpdate:
-      return bn == 256 ? launch_instance<kStageUpdate, 256>(l, grid, s)
-                       : launch_instance<kStageUpdate, 128>(l, grid, s);
+      return launch_instance<kStageUpdate>(l, pair_tiles, sms, s);
     default:
       return cudaErrorInvalidValue;
   }

@@ -199,6 +199,97 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
   if (L.wait_prior) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ apply
+// The tail of the Muon step ("Muon Custom Sizing 实战", section 四: decay
+// lr*wd on the parameter, then the NS result added with alpha = -lr * rescale;
+// "parameter-golf train_gpt.py 源码精读", section 分布式细节: the rescale
+// max(1, m/n)^0.5):  p <- (1 - lr wd) p - lr_eff O, with O the bf16 NS result
+// transposed back when rows > cols.  Same block layout as the prologue.
+template <bool TO_PARAM>
+__global__ void __launch_bounds__(256) apply_kernel(const __grid_constant__ ApplyLaunch L) {
+  __shared__ float stage_tile[64][65];
+  int gi = 0;
+  while (gi + 1 < L.n_groups && static_cast<int>(blockIdx.x) >= L.grp[gi + 1].block_begin) ++gi;
+  const ApplyGroup& A = L.grp[gi];
+  const int local = blockIdx.x - A.block_begin;
+  const int mat = local / A.nparts;
+  const int part = local - mat * A.nparts;
+  const int r = A.r, c = A.c;
+  const bool tall = r > c;
+  const int tiles_c = (c + 63) / 64;
+  const int ntiles = ((r + 63) / 64) * tiles_c;
+  const size_t moff = static_cast<size_t>(mat) * r * c;
+  const int m = tall ? c : r;
+  const __nv_bfloat16* om = A.o + static_cast<size_t>(mat) * m * A.ldx;
+  const int tid = threadIdx.x;
+  const int ty = tid >> 3;
+  const int tx = (tid & 7) * 8;
+  const bool cvec = (c & 7) == 0;
+
+  for (int tile = part; tile < ntiles; tile += A.nparts) {
+    const int tr = tile / tiles_c;
+    const int tc = tile - tr * tiles_c;
+    const int cc = tc * 64 + tx;
+    const int valid = max(0, min(8, c - cc));
+    float pv[2][8], ov[2][8];
+    if (TO_PARAM) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int rr = tr * 64 + ty + 32 * h;
+        if (rr < r && valid > 0)
+          load_f8(A.param + moff + static_cast<size_t>(rr) * c + cc, cvec && valid == 8, valid,
+                  pv[h]);
+      }
+    }
+    if (!tall) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int rr = tr * 64 + ty + 32 * h;
+        if (rr < r && valid > 0)
+          load_g8(om + static_cast<size_t>(rr) * A.ldx + cc, MUON_BF16, 0, valid == 8, valid,
+                  ov[h]);
+      }
+    } else {
+      // O row = original column, O column = original row: transpose the tile
+      const int xc = tr * 64 + tx;
+      const int xvalid = max(0, min(8, r - xc));
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int xr = tc * 64 + ty + 32 * h;
+        float v[8];
+        if (xr < c && xvalid > 0)
+          load_g8(om + static_cast<size_t>(xr) * A.ldx + xc, MUON_BF16, 0, xvalid == 8, xvalid, v);
+        else
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) stage_tile[ty + 32 * h][tx + e] = v[e];
+      }
+      __syncthreads();
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ov[h][e] = stage_tile[tx + e][ty + 32 * h];
+      __syncthreads();
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int rr = tr * 64 + ty + 32 * h;
+      if (rr < r && valid > 0) {
+        const size_t idx = moff + static_cast<size_t>(rr) * c + cc;
+        if (TO_PARAM) {
+          float nv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) nv[e] = fmaf(-A.lr_eff, ov[h][e], A.decay * pv[h][e]);
+          store_f8(A.param + idx, cvec && valid == 8, valid, nv);
+        } else {
+          store_bf8(A.out + idx, cvec && valid == 8, valid, ov[h]);
+        }
+      }
+    }
+  }
+}
+
 template <int MODE>
 cudaError_t launch_mode(const PrologueLaunch& l, bool pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
@@ -215,6 +306,14 @@ cudaError_t launch_mode(const PrologueLaunch& l, bool pdl, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t launch_apply(const ApplyLaunch& l, bool to_param, cudaStream_t s) {
+  if (to_param)
+    apply_kernel<true><<<l.total_blocks, 256, 0, s>>>(l);
+  else
+    apply_kernel<false><<<l.total_blocks, 256, 0, s>>>(l);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prologue(const PrologueLaunch& l, int mode, bool pdl, cudaStream_t s) {
   switch (mode) {

@@ -55,7 +55,10 @@ def _rand(shape, std, dtype, seed):
                                        ((1, 300, 520), torch.float32),
                                        ((2, 520, 300), torch.bfloat16)])
 def test_prologue_writes_u_then_gram_and_poly(shape, gdt):
-    """steps=1 leaves X0 = bf16(u or u^T), A = s^2 X0 X0^T and B = bA + cA^2 in the workspace."""
+    """steps=1 leaves X0 = bf16(u or u^T), A = s^2 X0 X0^T and B' = aI + bA + cA^2 in the workspace.
+
+    (The polynomial stage folds the a X term of the update into its output, so
+    the update is the single product B' X.)"""
     b, r, c = shape
     m, n = min(r, c), max(r, c)
     ldx, lda = (n + 7) // 8 * 8, (m + 7) // 8 * 8
@@ -86,7 +89,7 @@ def test_prologue_writes_u_then_gram_and_poly(shape, gdt):
         A_ref = s * s * (x @ x.T)
         assert rel(f64(A[i]), A_ref) < 8e-3
         a_ = f64(A[i])
-        B_ref = muon.COEFFS[1] * a_ + muon.COEFFS[2] * (a_ @ a_)
+        B_ref = muon.COEFFS[0] * np.eye(m) + muon.COEFFS[1] * a_ + muon.COEFFS[2] * (a_ @ a_)
         assert rel(f64(Bm[i]), B_ref) < 2e-2
 
 
@@ -283,7 +286,8 @@ def test_launch_count_and_trace():
     muon.trace_begin(64)
     muon.ns5(G)
     recs = muon.trace_end()
-    assert muon.kernel_launch_count() - n0 == 1 + 3 * 5
+    assert muon.kernel_launch_count() - n0 == 1 + 3 * 5 + 1
     kinds = [r["kind"] for r in recs]
-    assert kinds[0] == "prologue" and kinds[-1] == "update_apply"
+    assert kinds[0] == "prologue" and kinds[-1] == "apply"
+    assert kinds[1:16] == ["gram", "poly", "update"] * 5
     assert all(r["ms"] > 0 for r in recs)
