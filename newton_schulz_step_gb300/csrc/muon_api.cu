@@ -322,7 +322,8 @@ muon_status build_gemm(GemmLaunch& L, const std::vector<GPlan*>& chunk, int stag
       ok = operand_tmap(&L.tm_a[i], ws + g.am, g.m, g.m, g.batch, g.lda, kTileM) &&
            operand_tmap(&L.tm_b[i], ws + g.am, g.m, g.m, g.batch, g.lda, kTileM) &&
            output_tmap(&L.tm_out[i], ws + g.bm, g.m, g.m, g.batch, g.lda, true) &&
-           output_tmap(&L.tm_mir[i], ws + g.bm, g.m, g.m, g.batch, g.lda, false);
+           output_tmap(&L.tm_mir[i], ws + g.bm, g.m, g.m, g.batch, g.lda, false) &&
+           output_tmap(&L.tm_in[i], ws + g.am, g.m, g.m, g.batch, g.lda, true);
     } else {                            // X' = s B' X
       ok = operand_tmap(&L.tm_a[i], ws + g.bm, g.m, g.m, g.batch, g.lda, kTileM) &&
            operand_tmap(&L.tm_b[i], xc, g.n, g.m, g.batch, g.ldx, 64) &&

@@ -38,17 +38,22 @@
 
 namespace muon {
 
+// Shared memory per CTA: the operand ring, the epilogue staging slots, barriers.
+// Poly reads its b A term through TMA into a third slot per warp, which it
+// pays for with one stage less in the ring (its MMA side waits least).
+template <int STAGE>
 struct GemmCfg {
   static constexpr int kBN = 256;
-  static constexpr int kStages = 4;
+  static constexpr int kStages = STAGE == kStagePoly ? 3 : 4;
   static constexpr int kABytes = kTileM * kTileK * 2;    // 16 KB: 128 rows x 128 B
   static constexpr int kBBytes = kBN * kTileK * 2;       // 32 KB
   static constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
   static constexpr int kTmemCols = 2 * kBN;              // two 128 x 256 fp32 accumulators
   static constexpr int kEpiWarps = 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
-  static constexpr int kSlotBytes = 4096;                     // per warp, per slot
-  static constexpr int kStagingBytes = kEpiWarps * 2 * kSlotBytes;
+  static constexpr int kSlots = STAGE == kStagePoly ? 3 : 2;  // per epilogue warp
+  static constexpr int kSlotBytes = 4096;
+  static constexpr int kStagingBytes = kEpiWarps * kSlots * kSlotBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmem = kStages * kStageBytes + kStagingBytes + kBarBytes + 1024;
 };
@@ -105,7 +110,7 @@ __device__ __forceinline__ int tile_stride() { return gridDim.x >> 1; }
 template <int STAGE>
 __device__ void run_producer(const GemmLaunch& L, uint8_t* smem, uint64_t* full, uint64_t* empty,
                              volatile int* abort_flag, int rank) {
-  using C = GemmCfg;
+  using C = GemmCfg<STAGE>;
   for (int p = 0; p < L.n_prob; ++p) {
     ptx::prefetch_tmap(&L.tm_a[p]);
     ptx::prefetch_tmap(&L.tm_b[p]);
@@ -173,7 +178,7 @@ template <int STAGE>
 __device__ void run_mma(const GemmLaunch& L, uint8_t* smem, uint64_t* full, uint64_t* empty,
                         uint64_t* acc_full, uint64_t* acc_empty, uint64_t* drain,
                         uint32_t tmem_base, volatile int* abort_flag, int rank) {
-  using C = GemmCfg;
+  using C = GemmCfg<STAGE>;
   constexpr bool kBmn = (STAGE >= kStageUpdate);
   constexpr uint32_t kIdesc = ptx::idesc_bf16_m128(C::kBN, kBmn);
   int stage = 0;
@@ -296,45 +301,57 @@ __device__ __forceinline__ void stage_row_sw64(uint8_t* blk, int r, const float 
 
 // ------------------------------------------------------------ epilogue warps
 // Warp w (2..5) owns TMEM lanes 32*(w&3).. (32 rows of the 128-row tile) and
-// walks the tile's 256 columns in 8 chunks of 32.
+// walks the tile's 256 columns in 8 chunks of 32.  Symmetric stages skip the
+// chunks wholly below the diagonal (their entries come from mirrors).
 template <int STAGE>
 __device__ void run_epilogue(const GemmLaunch& L, uint64_t* acc_full, uint64_t* acc_empty,
-                             uint32_t tmem_base, uint8_t* staging, volatile int* abort_flag,
-                             int warp, int lane, int rank) {
-  using C = GemmCfg;
+                             uint64_t* in_bar, uint32_t tmem_base, uint8_t* staging,
+                             volatile int* abort_flag, int warp, int lane, int rank) {
+  using C = GemmCfg<STAGE>;
   constexpr int kChunks = C::kBN / 32;
   constexpr bool kSym = STAGE <= kStagePoly;
-  // the Poly operand ring needs static indices: full unroll
+  constexpr bool kPoly = STAGE == kStagePoly;
   const int quarter = warp & 3;
-  uint8_t* my_slots = staging + quarter * 2 * C::kSlotBytes;
+  uint8_t* my_slots = staging + quarter * C::kSlots * C::kSlotBytes;
+  uint64_t* my_in = in_bar + quarter * C::kSlots;
   int acc = 0;
   uint32_t acc_phase = 0;
-  int slot = 0;
+  int slot = 0;             // next staging slot (ring of kSlots)
+  uint32_t in_par = 0;      // Poly: parity of each slot's next input load
   for (int t = first_tile(); t < L.total_tiles; t += tile_stride()) {
     __syncwarp();
     const Tile tl = decode_tile<STAGE>(L, t, rank);
     const GemmProblem& P = L.prob[tl.prob];
     const CUtensorMap* tm_out = &L.tm_out[tl.prob];
     const CUtensorMap* tm_mir = &L.tm_mir[tl.prob];
+    const CUtensorMap* tm_in = &L.tm_in[tl.prob];
     float s = 1.f;
     if (STAGE != kStagePoly && P.first_round)
       s = inv_fro_norm(P.parts + static_cast<size_t>(tl.mat) * P.nparts, P.nparts, L.eps, lane);
     const int i0 = tl.tm * kTileM + quarter * 32;  // first row of this warp
-    const int i = i0 + lane;
-    const bool rows_live = i0 < P.m;                // warp-uniform
     const int ncols = kSym ? P.m : P.n;
     const int jt = tl.tn * C::kBN;
-
-    // Poly: the b A term, loaded two chunks ahead (row i of A, 64 bytes per chunk)
-    uint32_t e[3][16];
-    const __nv_bfloat16* arow =
-        P.a_mat + static_cast<size_t>(tl.mat) * P.m * P.lda +
-        static_cast<size_t>(i < P.m ? i : 0) * P.lda;
-    if (STAGE == kStagePoly && i < P.m) {
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch)
-        if (jt + 32 * ch < ncols) load_row32(arow + jt + 32 * ch, ncols - jt - 32 * ch, e[ch]);
+    // live chunks: c_lo <= ch < c_hi (rows in range, columns in range, and for
+    // symmetric stages not wholly below the diagonal)
+    int c_lo = 0, c_hi = 0;
+    if (i0 < P.m) {
+      c_hi = min(kChunks, (ncols - jt + 31) / 32);
+      if (kSym) c_lo = max(0, (i0 - jt) / 32);
     }
+    // Poly: the first two live chunks' A blocks into their slots
+    if constexpr (kPoly) {
+      if (lane == 0) {
+        for (int k = 0; k < 2 && c_lo + k < c_hi; ++k) {
+          const int sl = (slot + k) % C::kSlots;
+          if (k == 0) ptx::bulk_wait_read<2>(); else ptx::bulk_wait_read<1>();
+          ptx::mbar_arrive_expect_tx(&my_in[sl], 2048);
+          ptx::tma_load_3d(my_slots + sl * C::kSlotBytes, tm_in, jt + 32 * (c_lo + k), i0, tl.mat,
+                           &my_in[sl]);
+        }
+      }
+      __syncwarp();
+    }
+
     const bool got = ptx::mbar_wait(&acc_full[acc], acc_phase, abort_flag);
     __syncwarp();
     if (!got) {
@@ -344,76 +361,90 @@ __device__ void run_epilogue(const GemmLaunch& L, uint64_t* acc_full, uint64_t* 
     ptx::tc_fence_after();
     const uint32_t tbase =
         tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * C::kBN);
-#pragma unroll
-    for (int ch = 0; ch < kChunks; ++ch) {
+    bool failed = false;
+#pragma unroll 1
+    for (int ch = c_lo; ch < c_hi; ++ch) {
       const int j0 = jt + ch * 32;
-      if (j0 >= ncols) break;  // warp-uniform
-      if constexpr (STAGE == kStagePoly) {
-        if (i < P.m && ch + 2 < kChunks && j0 + 64 < ncols)
-          load_row32(arow + j0 + 64, ncols - j0 - 64, e[(ch + 2) % 3]);
+      uint8_t* blk = my_slots + slot * C::kSlotBytes;
+      uint8_t* mir = blk + 2048;
+      uint32_t ev[16];
+      if constexpr (kPoly) {
+        const uint32_t par = (in_par >> slot) & 1u;
+        if (!ptx::mbar_wait(&my_in[slot], par, abort_flag)) failed = true;
+        in_par ^= 1u << slot;
+        __syncwarp();
+        // row `lane` of the A block, 64-byte swizzled like the output blocks
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 w = *reinterpret_cast<const uint4*>(blk + sw64(lane, 8 * q));
+          ev[4 * q + 0] = w.x;
+          ev[4 * q + 1] = w.y;
+          ev[4 * q + 2] = w.z;
+          ev[4 * q + 3] = w.w;
+        }
+      } else {
+        // the slot's previous bulk store (two chunks ago) has read its data
+        if (lane == 0) ptx::bulk_wait_read<1>();
       }
       __syncwarp();
       uint32_t v[32];
       ptx::tmem_ld32(tbase + static_cast<uint32_t>(ch * 32), v);
       ptx::tmem_ld_wait();
-      // symmetric stages: blocks wholly below the diagonal belong to the mirror
-      // of another block and are skipped
-      const bool live = rows_live && !(kSym && j0 < i0);
-      if (live) {
-        float val[32];
-        if constexpr (STAGE == kStageGram) {
+      float val[32];
+      if constexpr (STAGE == kStageGram) {
 #pragma unroll
-          for (int q = 0; q < 32; ++q) val[q] = __uint_as_float(v[q]) * (s * s);
-        } else if constexpr (STAGE == kStagePoly) {
-          const uint32_t(&ev)[16] = e[ch % 3];
+        for (int q = 0; q < 32; ++q) val[q] = __uint_as_float(v[q]) * (s * s);
+      } else if constexpr (kPoly) {
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            val[2 * q] = fmaf(L.c, __uint_as_float(v[2 * q]), L.b * bf_lo(ev[q]));
-            val[2 * q + 1] = fmaf(L.c, __uint_as_float(v[2 * q + 1]), L.b * bf_hi(ev[q]));
-          }
-          // B' = a I + b A + c A A: the update then needs no a X term
-          if (j0 == i0) {
-#pragma unroll
-            for (int q = 0; q < 32; ++q) val[q] += (q == lane) ? L.a : 0.f;
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < 32; ++q) val[q] = s * __uint_as_float(v[q]);
+        for (int q = 0; q < 16; ++q) {
+          val[2 * q] = fmaf(L.c, __uint_as_float(v[2 * q]), L.b * bf_lo(ev[q]));
+          val[2 * q + 1] = fmaf(L.c, __uint_as_float(v[2 * q + 1]), L.b * bf_hi(ev[q]));
         }
-
-        // the slot's previous bulk store (two chunks ago) has read its data
-        if (lane == 0) ptx::bulk_wait_read<1>();
-        __syncwarp();
-        uint8_t* blk = my_slots + slot * C::kSlotBytes;
-        uint8_t* mir = blk + 2048;
-        const bool diag = kSym && j0 == i0;
-        if (!diag) {
-          stage_row_sw64(blk, lane, val);
-          if constexpr (kSym) {
+        // B' = a I + b A + c A A: the update then needs no a X term
+        if (j0 == i0) {
 #pragma unroll
-            for (int q = 0; q < 32; ++q)
-              *reinterpret_cast<__nv_bfloat16*>(mir + q * 64 + lane * 2) =
-                  __float2bfloat16_rn(val[q]);
-          }
-        } else {
-          // diagonal block: assemble it whole; entry (r, c) with c >= r comes
-          // from thread r, its mirror (c, r) from the same value
+          for (int q = 0; q < 32; ++q) val[q] += (q == lane) ? L.a : 0.f;
+        }
+      } else {
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const __nv_bfloat16 h = __float2bfloat16_rn(val[q]);
-            if (q >= lane) *reinterpret_cast<__nv_bfloat16*>(blk + sw64(lane, q)) = h;
-            if (q > lane) *reinterpret_cast<__nv_bfloat16*>(blk + sw64(q, lane)) = h;
-          }
-        }
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          ptx::tma_store_3d(tm_out, j0, i0, tl.mat, blk);
-          if (kSym && !diag) ptx::tma_store_3d(tm_mir, i0, j0, tl.mat, mir);
-          ptx::bulk_commit();
-        }
-        slot ^= 1;
+        for (int q = 0; q < 32; ++q) val[q] = s * __uint_as_float(v[q]);
       }
+
+      const bool diag = kSym && j0 == i0;
+      if (!diag) {
+        stage_row_sw64(blk, lane, val);
+        if constexpr (kSym) {
+#pragma unroll
+          for (int q = 0; q < 32; ++q)
+            *reinterpret_cast<__nv_bfloat16*>(mir + q * 64 + lane * 2) =
+                __float2bfloat16_rn(val[q]);
+        }
+      } else {
+        // diagonal block: assemble it whole; entry (r, c) with c >= r comes
+        // from thread r, its mirror (c, r) from the same value
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          const __nv_bfloat16 h = __float2bfloat16_rn(val[q]);
+          if (q >= lane) *reinterpret_cast<__nv_bfloat16*>(blk + sw64(lane, q)) = h;
+          if (q > lane) *reinterpret_cast<__nv_bfloat16*>(blk + sw64(q, lane)) = h;
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_3d(tm_out, j0, i0, tl.mat, blk);
+        if (kSym && !diag) ptx::tma_store_3d(tm_mir, i0, j0, tl.mat, mir);
+        ptx::bulk_commit();
+        // Poly: the A block two live chunks ahead goes into the slot whose
+        // store was issued one chunk ago
+        if (kPoly && ch + 2 < c_hi) {
+          const int sl = (slot + 2) % C::kSlots;
+          ptx::bulk_wait_read<1>();
+          ptx::mbar_arrive_expect_tx(&my_in[sl], 2048);
+          ptx::tma_load_3d(my_slots + sl * C::kSlotBytes, tm_in, j0 + 64, i0, tl.mat, &my_in[sl]);
+        }
+      }
+      slot = (slot + 1) % C::kSlots;
     }
     ptx::tc_fence_before();
     __syncwarp();
@@ -422,17 +453,21 @@ __device__ void run_epilogue(const GemmLaunch& L, uint64_t* acc_full, uint64_t* 
       acc = 0;
       acc_phase ^= 1u;
     }
+    if (failed) {
+      record_failure(L, abort_flag, kErrTimeoutEpilogue);
+      break;
+    }
   }
-  // all bulk stores of this warp are complete before the CTA exits
+  // all bulk copies of this warp are complete before the CTA exits
   if (lane == 0) ptx::bulk_wait<0>();
   __syncwarp();
 }
 
 // ------------------------------------------------------------ kernel
 template <int STAGE>
-__global__ void __launch_bounds__(GemmCfg::kThreads, 1)
+__global__ void __launch_bounds__(GemmCfg<STAGE>::kThreads, 1)
     ns_gemm_kernel(const __grid_constant__ GemmLaunch L) {
-  using C = GemmCfg;
+  using C = GemmCfg<STAGE>;
   extern __shared__ uint8_t smem_raw[];
   // every CTA of the cluster gets the same aligned offsets (multicast targets)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -444,12 +479,16 @@ __global__ void __launch_bounds__(GemmCfg::kThreads, 1)
   uint64_t* acc_full = bars + 2 * C::kStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* in_bar = drain + 1;  // Poly: one per epilogue warp and slot
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(in_bar + C::kEpiWarps * C::kSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int rank = static_cast<int>(ptx::cluster_ctarank());
+  // the next stage may be scheduled now; it takes an SM only once this CTA has
+  // left it, and waits for this grid to finish before reading its output
+  ptx::griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -461,6 +500,7 @@ __global__ void __launch_bounds__(GemmCfg::kThreads, 1)
       ptx::mbar_init(&acc_empty[s], C::kEpiWarps);
     }
     ptx::mbar_init(drain, 1);
+    for (int k = 0; k < C::kEpiWarps * C::kSlots; ++k) ptx::mbar_init(&in_bar[k], 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -474,6 +514,8 @@ __global__ void __launch_bounds__(GemmCfg::kThreads, 1)
   ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // setup above overlapped the previous stage's tail; its output is read below
+  ptx::griddep_wait();
 
   if (warp == 0) {
     if (lane == 0) run_producer<STAGE>(L, smem, full, empty, abort_flag, rank);
@@ -482,8 +524,8 @@ __global__ void __launch_bounds__(GemmCfg::kThreads, 1)
       run_mma<STAGE>(L, smem, full, empty, acc_full, acc_empty, drain, tmem_base, abort_flag,
                      rank);
   } else {
-    run_epilogue<STAGE>(L, acc_full, acc_empty, tmem_base, staging, abort_flag, warp, lane,
-                        rank);
+    run_epilogue<STAGE>(L, acc_full, acc_empty, in_bar, tmem_base, staging, abort_flag, warp,
+                        lane, rank);
   }
 
   __syncwarp();
@@ -500,22 +542,24 @@ __global__ void __launch_bounds__(GemmCfg::kThreads, 1)
 // ------------------------------------------------------------ launchers
 template <int STAGE>
 static cudaError_t launch_instance(const GemmLaunch& l, int pair_tiles, int sms, cudaStream_t s) {
-  constexpr int kSmem = GemmCfg::kSmem;
+  constexpr int kSmem = GemmCfg<STAGE>::kSmem;
   static int max_clusters[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(GemmCfg::kThreads);
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.blockDim = dim3(GemmCfg<STAGE>::kThreads);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;  // occupancy query: cluster shape only
   // clusters that fit on the device at once (one CTA per SM), queried once
   int n = dev < 64 ? max_clusters[dev] : 0;
   if (n == 0) {
@@ -530,10 +574,11 @@ static cudaError_t launch_instance(const GemmLaunch& l, int pair_tiles, int sms,
   }
   const int clusters = pair_tiles < n ? pair_tiles : n;
   cfg.gridDim = dim3(2 * clusters);
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, ns_gemm_kernel<STAGE>, l);
 }
 
-int gemm_smem_bytes() { return GemmCfg::kSmem; }
+int gemm_smem_bytes() { return GemmCfg<kStageUpdate>::kSmem; }
 
 cudaError_t launch_gemm(const GemmLaunch& l, int stage, int pair_tiles, int sms, cudaStream_t s) {
   switch (stage) {

@@ -99,6 +99,8 @@ template <int MODE>
 __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ PrologueLaunch L) {
   __shared__ float stage_tile[64][65];
   __shared__ float red[8];
+  // the first Gram stage may be scheduled once every block here has started
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int gi = 0;
   while (gi + 1 < L.n_groups && static_cast<int>(blockIdx.x) >= L.grp[gi + 1].block_begin) ++gi;
   const PrologueGroup& A = L.grp[gi];
@@ -208,6 +210,8 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
 template <bool TO_PARAM>
 __global__ void __launch_bounds__(256) apply_kernel(const __grid_constant__ ApplyLaunch L) {
   __shared__ float stage_tile[64][65];
+  // launched as a programmatic dependent of the last update: its output is O
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int gi = 0;
   while (gi + 1 < L.n_groups && static_cast<int>(blockIdx.x) >= L.grp[gi + 1].block_begin) ++gi;
   const ApplyGroup& A = L.grp[gi];
@@ -308,11 +312,17 @@ cudaError_t launch_mode(const PrologueLaunch& l, bool pdl, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_apply(const ApplyLaunch& l, bool to_param, cudaStream_t s) {
-  if (to_param)
-    apply_kernel<true><<<l.total_blocks, 256, 0, s>>>(l);
-  else
-    apply_kernel<false><<<l.total_blocks, 256, 0, s>>>(l);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(l.total_blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return to_param ? cudaLaunchKernelEx(&cfg, apply_kernel<true>, l)
+                  : cudaLaunchKernelEx(&cfg, apply_kernel<false>, l);
 }
 
 cudaError_t launch_prologue(const PrologueLaunch& l, int mode, bool pdl, cudaStream_t s) {
