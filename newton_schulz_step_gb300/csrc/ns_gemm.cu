@@ -19,20 +19,24 @@
 // A[j][k] is then read K-major like the first; only the Update's X operand
 // (contraction over X's rows) is MN-major.
 //
-// Kernel shape: persistent clusters of two CTAs, one CTA per SM, 192 threads:
+// Kernel shape: persistent clusters of two CTAs (a CTA pair), one CTA per SM,
+// 192 threads:
 //   warp 0      TMA producer (one lane) into a ring of swizzled smem stages
-//   warp 1      TMEM allocator and tcgen05.mma issuer (one lane)
+//   warp 1      TMEM allocator; in the even CTA also the tcgen05.mma issuer
 //   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator, fp32 math, 32 x 32
 //               blocks staged in shared memory and written by TMA bulk stores
 //               (Gram and Poly also store each block's mirror the same way)
-// Each CTA computes a 128 x 256 tile; the two CTAs of a cluster take tile rows
-// 2p and 2p+1 of the same tile column, so they need the same B operand: each
-// loads half of it and multicasts that half to both, halving the B traffic
-// out of L2.  With 256-wide tile columns the two rows of a pair also have the
-// same set of upper-triangle tiles, so symmetric stages pair up exactly.  A
-// stage slot is reused only after both CTAs' MMAs have read it (each MMA warp
-// commits to the empty barriers of both CTAs).  The accumulator is double
-// buffered in TMEM so the epilogue of one tile overlaps the MMAs of the next.
+// The pair computes a 256 x 256 tile with cta_group::2 MMAs (M = 256): CTA r
+// holds tile rows 2p + r (128 rows of A) and the r-th 128-column half of B in
+// its own shared memory, and receives its 128 rows of the result in its own
+// TMEM.  Each SM therefore receives 32 KB of operands per 64-deep k-block for
+// 128 x 256 x 64 of MMA work.  Both CTAs' copies complete on the even CTA's
+// stage barrier; its MMA commits free the slot in both CTAs; both CTAs'
+// epilogue warps release the accumulator on the even CTA's barrier.  With
+// 256-wide tile columns the two rows of a pair have the same set of
+// upper-triangle tiles, so symmetric stages pair up exactly.  The accumulator
+// is double buffered in TMEM so the epilogue of one tile overlaps the MMAs of
+// the next.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -43,11 +47,11 @@ namespace muon {
 // pays for with one stage less in the ring (its MMA side waits least).
 template <int STAGE>
 struct GemmCfg {
-  static constexpr int kBN = 256;
-  static constexpr int kStages = STAGE == kStagePoly ? 3 : 4;
+  static constexpr int kBN = 256;                        // pair tile: 256 x 256
+  static constexpr int kStages = STAGE == kStagePoly ? 5 : 6;
   static constexpr int kABytes = kTileM * kTileK * 2;    // 16 KB: 128 rows x 128 B
-  static constexpr int kBBytes = kBN * kTileK * 2;       // 32 KB
-  static constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
+  static constexpr int kBBytes = (kBN / 2) * kTileK * 2; // 16 KB: this CTA's half of B
+  static constexpr int kStageBytes = kABytes + kBBytes;  // 32 KB
   static constexpr int kTmemCols = 2 * kBN;              // two 128 x 256 fp32 accumulators
   static constexpr int kEpiWarps = 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
@@ -57,7 +61,6 @@ struct GemmCfg {
   static constexpr int kBarBytes = 256;
   static constexpr int kSmem = kStages * kStageBytes + kStagingBytes + kBarBytes + 1024;
 };
-constexpr uint16_t kPairMask = 0x3;
 
 struct Tile {
   int prob, mat, tm, tn;  // tm: this CTA's tile row (2 * pair row + cluster rank)
@@ -119,13 +122,14 @@ __device__ void run_producer(const GemmLaunch& L, uint8_t* smem, uint64_t* full,
   uint32_t phase = 0;
   uint32_t armed = 0, armed_parity = 0;
   bool ok = true;
+  const uint32_t leader_full0 = ptx::mapa_shared(ptx::smem_u32(full), 0);
   for (int t = first_tile(); ok && t < L.total_tiles; t += tile_stride()) {
     const Tile tl = decode_tile<STAGE>(L, t, rank);
     const GemmProblem& P = L.prob[tl.prob];
     const CUtensorMap* ta = &L.tm_a[tl.prob];
     const CUtensorMap* tb = &L.tm_b[tl.prob];
     for (int kb = 0; kb < P.k_blocks; ++kb) {
-      // both CTAs' MMAs must be done with this slot: the peer's half lands here too
+      // the pair's MMAs (issued by the even CTA) are done with this slot
       if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
         record_failure(L, abort_flag, kErrTimeoutProducer);
         ok = false;
@@ -133,24 +137,21 @@ __device__ void run_producer(const GemmLaunch& L, uint8_t* smem, uint64_t* full,
       }
       uint8_t* sa = smem + stage * C::kStageBytes;
       uint8_t* sb = sa + C::kABytes;
-      ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+      // both CTAs' copies complete on the even CTA's barrier for this slot
+      const uint32_t bar = leader_full0 + stage * 8;
+      if (rank == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
       // operand A: this CTA's 128 rows x 64 k-columns
-      ptx::tma_load_3d(sa, ta, kb * kTileK, tl.tm * kTileM, tl.mat, &full[stage]);
+      ptx::tma_load_3d_pair(sa, ta, kb * kTileK, tl.tm * kTileM, tl.mat, bar);
       if (STAGE >= kStageUpdate) {
-        // operand B = X[k][j], MN-major: 4 slabs of 64 columns x 64 k-rows; this
-        // CTA loads slabs 2*rank, 2*rank+1 for both CTAs
+        // operand B = X[k][j], MN-major: this CTA's 128 columns as 2 slabs of
+        // 64 columns x 64 k-rows
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int slab = 2 * rank + q;
-          ptx::tma_load_3d_multicast(sb + slab * (64 * kTileK * 2), tb, tl.tn * C::kBN + slab * 64,
-                                     kb * kTileK, tl.mat, &full[stage], kPairMask);
-        }
+        for (int q = 0; q < 2; ++q)
+          ptx::tma_load_3d_pair(sb + q * (64 * kTileK * 2), tb, tl.tn * C::kBN + rank * 128 + q * 64,
+                                kb * kTileK, tl.mat, bar);
       } else {
-        // operand B: 256 rows (tile col tn) x 64 k-columns, K-major; this CTA
-        // loads rows 128*rank .. +127 for both CTAs
-        ptx::tma_load_3d_multicast(sb + rank * C::kABytes, tb, kb * kTileK,
-                                   tl.tn * C::kBN + rank * kTileM, tl.mat, &full[stage],
-                                   kPairMask);
+        // operand B: this CTA's 128 of the tile column's 256 rows, K-major
+        ptx::tma_load_3d_pair(sb, tb, kb * kTileK, tl.tn * C::kBN + rank * kTileM, tl.mat, bar);
       }
       armed |= 1u << stage;
       armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -160,35 +161,32 @@ __device__ void run_producer(const GemmLaunch& L, uint8_t* smem, uint64_t* full,
       }
     }
   }
-  // Before exit: every armed stage's copies (own and the peer's) have landed,
-  // and both CTAs' MMAs have released it, so no multicast copy or remote
-  // commit arrival can still be on its way to this CTA.
-  for (int s = 0; s < C::kStages; ++s) {
-    if (armed & (1u << s)) {
-      const uint32_t par = (armed_parity >> s) & 1u;
-      if (!ptx::mbar_wait(&full[s], par, nullptr)) record_failure(L, abort_flag, kErrTimeoutDrain);
-      if (!ptx::mbar_wait(&empty[s], par, nullptr))
+  // Before exit: the pair's MMAs have released every armed stage, so its copies
+  // landed and no commit arrival can still be on its way to this CTA.
+  for (int s = 0; s < C::kStages; ++s)
+    if (armed & (1u << s))
+      if (!ptx::mbar_wait(&empty[s], (armed_parity >> s) & 1u, nullptr))
         record_failure(L, abort_flag, kErrTimeoutDrain);
-    }
-  }
 }
 
 // ------------------------------------------------------------ MMA issuer
+// Runs in the even CTA of the pair only.
 template <int STAGE>
 __device__ void run_mma(const GemmLaunch& L, uint8_t* smem, uint64_t* full, uint64_t* empty,
                         uint64_t* acc_full, uint64_t* acc_empty, uint64_t* drain,
-                        uint32_t tmem_base, volatile int* abort_flag, int rank) {
+                        uint32_t tmem_base, volatile int* abort_flag) {
   using C = GemmCfg<STAGE>;
   constexpr bool kBmn = (STAGE >= kStageUpdate);
-  constexpr uint32_t kIdesc = ptx::idesc_bf16_m128(C::kBN, kBmn);
+  constexpr uint32_t kIdesc = ptx::idesc_bf16(2 * kTileM, C::kBN, kBmn);
   int stage = 0;
   uint32_t phase = 0;
   int acc = 0;
   uint32_t acc_phase = 0;
   bool ok = true;
   for (int t = first_tile(); ok && t < L.total_tiles; t += tile_stride()) {
-    const Tile tl = decode_tile<STAGE>(L, t, rank);
+    const Tile tl = decode_tile<STAGE>(L, t, 0);
     const int kblocks = L.prob[tl.prob].k_blocks;
+    // both CTAs' epilogues have drained this accumulator
     if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
       record_failure(L, abort_flag, kErrTimeoutMma);
       break;
@@ -212,24 +210,24 @@ __device__ void run_mma(const GemmLaunch& L, uint8_t* smem, uint64_t* full, uint
         // groups 1024 B apart along K; a K=16 slice is 16 rows = 2048 B on.
         const uint64_t db = kBmn ? ptx::smem_desc_sw128(sb + k * 2048, 64 * kTileK * 2, 1024)
                                  : ptx::smem_desc_sw128(sb + k * 32, 16, 1024);
-        ptx::mma_bf16(d_tmem, da, db, kIdesc, (kb | k) != 0 ? 1u : 0u);
+        ptx::mma_bf16_pair(d_tmem, da, db, kIdesc, (kb | k) != 0 ? 1u : 0u);
       }
       // frees the slot in both CTAs once these MMAs have read it
-      ptx::mma_commit_multicast(&empty[stage], kPairMask);
+      ptx::mma_commit_pair(&empty[stage]);
       if (++stage == C::kStages) {
         stage = 0;
         phase ^= 1u;
       }
     }
     if (!ok) break;
-    ptx::mma_commit(&acc_full[acc]);
+    ptx::mma_commit_pair(&acc_full[acc]);
     if (++acc == 2) {
       acc = 0;
       acc_phase ^= 1u;
     }
   }
   // Every MMA issued by this thread completes before TMEM is released.
-  ptx::mma_commit(drain);
+  ptx::mma_commit_pair(drain, 1);
   if (!ptx::mbar_wait(drain, 0, nullptr)) record_failure(L, abort_flag, kErrTimeoutDrain);
 }
 
@@ -448,7 +446,8 @@ __device__ void run_epilogue(const GemmLaunch& L, uint64_t* acc_full, uint64_t* 
     }
     ptx::tc_fence_before();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
+    // release the accumulator on the even CTA's barrier (the MMA issuer's)
+    if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&acc_empty[acc]), 0));
     if (++acc == 2) {
       acc = 0;
       acc_phase ^= 1u;
@@ -469,7 +468,7 @@ __global__ void __launch_bounds__(GemmCfg<STAGE>::kThreads, 1)
     ns_gemm_kernel(const __grid_constant__ GemmLaunch L) {
   using C = GemmCfg<STAGE>;
   extern __shared__ uint8_t smem_raw[];
-  // every CTA of the cluster gets the same aligned offsets (multicast targets)
+  // both CTAs of the pair get the same aligned offsets (the pair MMA reads both)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* staging = smem + C::kStages * C::kStageBytes;
@@ -492,12 +491,12 @@ __global__ void __launch_bounds__(GemmCfg<STAGE>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 2);  // one commit from each CTA's MMA warp
+      ptx::mbar_init(&full[s], 1);   // the even CTA's expect_tx (+ both CTAs' bytes)
+      ptx::mbar_init(&empty[s], 1);  // the pair MMA commit
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&acc_full[s], 1);
-      ptx::mbar_init(&acc_empty[s], C::kEpiWarps);
+      ptx::mbar_init(&acc_empty[s], 2 * C::kEpiWarps);  // both CTAs' epilogue warps
     }
     ptx::mbar_init(drain, 1);
     for (int k = 0; k < C::kEpiWarps * C::kSlots; ++k) ptx::mbar_init(&in_bar[k], 1);
@@ -505,12 +504,12 @@ __global__ void __launch_bounds__(GemmCfg<STAGE>::kThreads, 1)
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(tmem_slot, C::kTmemCols);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc_pair(tmem_slot, C::kTmemCols);
+    ptx::tmem_relinquish_pair();
   }
   __syncwarp();
   ptx::tc_fence_before();
-  // both CTAs' barriers exist before either multicasts into the other
+  // both CTAs' barriers exist before either's copies signal the other's
   ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
@@ -520,9 +519,8 @@ __global__ void __launch_bounds__(GemmCfg<STAGE>::kThreads, 1)
   if (warp == 0) {
     if (lane == 0) run_producer<STAGE>(L, smem, full, empty, abort_flag, rank);
   } else if (warp == 1) {
-    if (lane == 0)
-      run_mma<STAGE>(L, smem, full, empty, acc_full, acc_empty, drain, tmem_base, abort_flag,
-                     rank);
+    if (lane == 0 && rank == 0)
+      run_mma<STAGE>(L, smem, full, empty, acc_full, acc_empty, drain, tmem_base, abort_flag);
   } else {
     run_epilogue<STAGE>(L, acc_full, acc_empty, in_bar, tmem_base, staging, abort_flag, warp,
                         lane, rank);
@@ -535,7 +533,7 @@ __global__ void __launch_bounds__(GemmCfg<STAGE>::kThreads, 1)
   ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+    ptx::tmem_dealloc_pair(tmem_base, C::kTmemCols);
   }
 }
 
