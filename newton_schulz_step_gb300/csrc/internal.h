@@ -108,6 +108,7 @@ struct GemmProblem {
   const float* parts;           // norm partials [batch, nparts]
   int nparts;
   int first_round;              // fold s = 1/(||u||_F + eps) in
+  int reverse;                  // walk this problem's matrices in descending order
 };
 
 struct GemmLaunch {

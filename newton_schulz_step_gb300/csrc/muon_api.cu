@@ -284,12 +284,15 @@ double stage_flops(const GPlan& g, int stage) {
 muon_status build_gemm(GemmLaunch& L, const std::vector<GPlan*>& chunk, int stage,
                        int cur, bool first_round, const Scalars& sc, uint8_t* ws) {
   std::memset(&L, 0, sizeof(L));
-  // heaviest problems first: their tiles are handed out first
+  // Order of the tile walk.  The update and Poly stages walk the groups by
+  // ascending n (matrices ascending); the Gram stage walks the exact reverse,
+  // so it reads first the X the previous update wrote last (still in L2), and
+  // its heaviest tiles (largest n = longest K) are handed out first.
   std::vector<GPlan*> order(chunk);
-  std::stable_sort(order.begin(), order.end(), [&](GPlan* x, GPlan* y) {
-    const StageShape sx = stage_shape(*x, stage), sy = stage_shape(*y, stage);
-    return sx.k_blocks > sy.k_blocks;
-  });
+  std::stable_sort(order.begin(), order.end(),
+                   [](GPlan* x, GPlan* y) { return x->n < y->n; });
+  const bool reverse = (stage == kStageGram);
+  if (reverse) std::reverse(order.begin(), order.end());
   int tiles = 0;
   for (size_t i = 0; i < order.size(); ++i) {
     const GPlan& g = *order[i];
@@ -312,6 +315,7 @@ muon_status build_gemm(GemmLaunch& L, const std::vector<GPlan*>& chunk, int stag
     P.parts = reinterpret_cast<const float*>(ws + g.parts);
     P.nparts = g.nparts;
     P.first_round = first_round ? 1 : 0;
+    P.reverse = reverse ? 1 : 0;
     bool ok = true;
     if (stage == kStageGram) {          // A = s^2 X X^T
       ok = operand_tmap(&L.tm_a[i], xc, g.n, g.m, g.batch, g.ldx, kTileM) &&
@@ -488,7 +492,8 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
     std::memset(&al, 0, sizeof(al));
     double bytes = 0;
     int blocks = 0;
-    for (size_t k = c0; k < std::min(big.size(), c0 + kMaxPrologueGroups); ++k) {
+    const size_t c1 = std::min(big.size(), c0 + kMaxPrologueGroups);
+    for (size_t k = c1; k-- > c0;) {  // the last update's final groups first
       const GPlan& g = *big[k];
       ApplyGroup& ag = al.grp[al.n_groups++];
       ag.o = reinterpret_cast<const __nv_bfloat16*>(ws + ((sc.steps & 1) ? g.x1 : g.x0));

@@ -79,6 +79,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmLaunch& L, int t, int rank
   r.prob = p;
   r.mat = local / P.tiles_per_mat;
   int w = local - r.mat * P.tiles_per_mat;
+  if (P.reverse) r.mat = P.batch - 1 - r.mat;
   int tp = P.tiles_m;  // out of range unless found (no stores then)
   if (STAGE >= kStageUpdate) {
     tp = w / P.tiles_n;
@@ -194,12 +195,13 @@ __device__ void run_mma(const GemmLaunch& L, uint8_t* smem, uint64_t* full, uint
     ptx::tc_fence_after();
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::kBN);
     for (int kb = 0; kb < kblocks; ++kb) {
+      // (the barrier orders the TMA writes before these MMA reads; no tcgen05
+      // fence is needed here)
       if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) {
         record_failure(L, abort_flag, kErrTimeoutMma);
         ok = false;
         break;
       }
-      ptx::tc_fence_after();
       const uint32_t sa = ptx::smem_u32(smem + stage * C::kStageBytes);
       const uint32_t sb = sa + C::kABytes;
 #pragma unroll
