@@ -18,3 +18,4 @@ from .muon_oracle import (  # noqa: F401
     newton_schulz5_batched,
     rescale_factor,
 )
+from .adam_oracle import ADAM_BETAS, ADAM_EPS, ADAM_LR, adam_step  # noqa: F401,E402
