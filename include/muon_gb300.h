@@ -154,6 +154,17 @@ muon_status muon_step_grouped(const muon_group* groups, int n_groups,
 muon_status muon_workspace_status(const void* workspace, size_t workspace_bytes,
                                   void* stream, int clear);
 
+/*
+ * Self-test of the device-side timeout path (no counterpart on the pages).
+ * Enqueues one kernel whose bounded wait, the same code every GEMM role waits
+ * with, is on a barrier that nothing completes; after `limit_us` (1..100000)
+ * it gives up and records the timeout in the workspace's status word, as a
+ * stalled GEMM would.  muon_workspace_status() then reports MUON_ERR_TIMEOUT.
+ * Nothing faults, hangs or is left pending on the GPU.
+ */
+muon_status muon_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int limit_us,
+                                       void* stream);
+
 /* Static English text for a status code. */
 const char* muon_status_string(muon_status status);
 

@@ -89,6 +89,8 @@ def load_library():
     L.muon_step_grouped.restype = ci
     L.muon_workspace_status.argtypes = [vp, sz, vp, ci]
     L.muon_workspace_status.restype = ci
+    L.muon_selftest_wait_timeout.argtypes = [vp, sz, ci, vp]
+    L.muon_selftest_wait_timeout.restype = ci
     L.muon_status_string.argtypes = [ci]
     L.muon_status_string.restype = ctypes.c_char_p
     L.muon_kernel_launch_count.argtypes = []
@@ -317,6 +319,13 @@ def workspace_status(workspace: Workspace, clear: bool = False, stream=None) -> 
     """Synchronise and read the workspace's sticky device error word (0 = ok, 4 = timeout)."""
     return int(load_library().muon_workspace_status(workspace.ptr, workspace.nbytes,
                                                     _stream_handle(stream), int(clear)))
+
+
+def selftest_wait_timeout(workspace: Workspace, limit_us: int = 1000, stream=None):
+    """Run the device-side bounded-wait timeout path once (see the C header)."""
+    _raise(load_library().muon_selftest_wait_timeout(workspace.ptr, workspace.nbytes, limit_us,
+                                                     _stream_handle(stream)),
+           "muon_selftest_wait_timeout")
 
 
 def kernel_launch_count() -> int:

@@ -138,5 +138,7 @@ cudaError_t launch_apply(const ApplyLaunch& l, bool to_param, cudaStream_t s);
 // CTA tiles each); the grid is sized from the device's SM count.
 cudaError_t launch_gemm(const GemmLaunch& l, int stage, int pair_tiles, int sms, cudaStream_t s);
 int gemm_smem_bytes();
+cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_ns,
+                                 cudaStream_t s);
 
 }  // namespace muon

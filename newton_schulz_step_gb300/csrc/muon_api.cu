@@ -628,6 +628,23 @@ muon_status muon_workspace_status(const void* workspace, size_t workspace_bytes,
   return word ? MUON_ERR_TIMEOUT : MUON_OK;
 }
 
+muon_status muon_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int limit_us,
+                                       void* stream) {
+  if (!workspace || workspace_bytes < kStatusBytes ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MUON_ERR_WORKSPACE;
+  if (limit_us < 1 || limit_us > 100000) return MUON_ERR_INVALID_ARG;
+  int sms = 0;
+  const muon_status s = current_device(&sms);
+  if (s != MUON_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = launch_wait_selftest(static_cast<unsigned int*>(workspace),
+                                             1000ull * static_cast<unsigned long long>(limit_us),
+                                             st);
+  g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+}
+
 const char* muon_status_string(muon_status status) {
   switch (status) {
     case MUON_OK:

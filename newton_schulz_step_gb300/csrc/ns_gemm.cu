@@ -539,6 +539,28 @@ __global__ void __launch_bounds__(GemmCfg<STAGE>::kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------ wait self-test
+// One thread waits on a barrier that nothing completes, through the same
+// bounded wait the GEMM roles use, with a short limit; the timeout is recorded
+// in the status word exactly as a GEMM role records one.
+__global__ void wait_selftest_kernel(unsigned int* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  ptx::mbar_init(&bar, 1);
+  abort_flag = 0;
+  ptx::fence_mbar_init();
+  if (!ptx::mbar_wait(&bar, 0, &abort_flag, limit_ns)) atomicOr(status, kErrTimeoutEpilogue);
+  // complete the barrier's phase so nothing is left pending
+  ptx::mbar_arrive(&bar);
+}
+
+cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_ns,
+                                 cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------ launchers
 template <int STAGE>
 static cudaError_t launch_instance(const GemmLaunch& l, int pair_tiles, int sms, cudaStream_t s) {

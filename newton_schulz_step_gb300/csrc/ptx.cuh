@@ -68,7 +68,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Wait until the phase with the given parity has completed.  Returns false on
 // timeout or when *abort_flag becomes non-zero (abort_flag may be null).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          const volatile int* abort_flag) {
+                                          const volatile int* abort_flag,
+                                          uint64_t timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   uint32_t spins = 0;
@@ -76,7 +77,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     if (mbar_try_wait(bar, parity)) return true;
     if ((++spins & 63u) == 0u) {
       if (abort_flag != nullptr && *abort_flag) return false;
-      if (globaltimer() - t0 > kWaitTimeoutNs) return false;
+      if (globaltimer() - t0 > timeout_ns) return false;
     }
   }
 }

@@ -119,6 +119,12 @@ def test_ns5_argument_errors(lib):
     assert f(0x1000, 1, 0x2000, 0, 64, 64, 5, A, B, C, 1e-7, 0x10000, 1 << 30, None) == OK
 
 
+def test_selftest_argument_errors(lib):
+    assert lib.muon_selftest_wait_timeout(None, 1024, 1000, None) == WORKSPACE
+    assert lib.muon_selftest_wait_timeout(0x10000, 1024, 0, None) == INVALID
+    assert lib.muon_selftest_wait_timeout(0x10000, 1024, 200000, None) == INVALID
+
+
 def test_workspace_status_argument_errors(lib):
     assert lib.muon_workspace_status(None, 1024, None, 0) == WORKSPACE
     assert lib.muon_workspace_status(0x10010, 1024, None, 0) == WORKSPACE

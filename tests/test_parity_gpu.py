@@ -291,3 +291,16 @@ def test_launch_count_and_trace():
     assert kinds[0] == "prologue" and kinds[-1] == "apply"
     assert kinds[1:16] == ["gram", "poly", "update"] * 5
     assert all(r["ms"] > 0 for r in recs)
+
+
+def test_device_timeout_is_reported_and_the_context_stays_usable():
+    """A bounded device wait that runs out is recorded and read back; no fault, no hang."""
+    ws = muon.Workspace(1 << 16)
+    assert muon.workspace_status(ws) == 0
+    muon.selftest_wait_timeout(ws, limit_us=2000)
+    assert muon.workspace_status(ws, clear=True) == 4     # MUON_ERR_TIMEOUT, then cleared
+    assert muon.workspace_status(ws) == 0
+    G = _rand((1, 128, 256), 1.0, torch.bfloat16, 3)
+    out = muon.ns5(G.to(DEV))                              # the context still works
+    torch.cuda.synchronize()
+    assert rel(f64(out[0]), oracle.newton_schulz5(f64(G[0]))) < NS_TOL
