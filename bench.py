@@ -323,6 +323,8 @@ def run_gpu(args, wl):
                                              "ms_per_step": kinds[name]["ms"] / args.steps}
                                       for name in ("prologue", "apply") if name in kinds}}
 
+    adam = time_adam(args, wl, dev, peaks) if wl.adam else None
+
     # end to end through the public API with host buffers: grads in, params out
     host_g = [G.cpu().pin_memory() for _, G, _ in tensors]
     host_p = [torch.empty(P.shape, dtype=P.dtype, pin_memory=True) for P, _, _ in tensors]
@@ -374,6 +376,7 @@ def run_gpu(args, wl):
             "kernels": {k: {"ms_per_step": v["ms"] / args.steps, "launches_per_step":
                             v["n"] / args.steps} for k, v in kinds.items()},
             "elementwise": elementwise,
+            "adam": adam,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clock,
         }
@@ -382,6 +385,43 @@ def run_gpu(args, wl):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def time_adam(args, wl, dev, peaks):
+    """The Adam half of the optimizer on the workload's non-matrix parameters
+    (embedding, head, scalars): one fused launch per step, timed on its own.
+    Not part of the Muon-step metric above; reported beside it."""
+    import torch
+
+    import newton_schulz_step_gb300 as muon
+    import workloads
+
+    sets = workloads.make_adam_set(wl, dev)
+    run = muon.AdamStep([(p, g, m, v, t.lr_scale, t.wd_scale) for t, p, g, m, v in sets],
+                        lr=muon.ADAM_LR, betas=muon.ADAM_BETAS, eps=muon.ADAM_EPS,
+                        weight_decay=0.0)
+    nbytes = sum(p.numel() * (12 + g.element_size() + 12) for _, p, g, m, v in sets)
+    stream = torch.cuda.current_stream()
+    t = wl.adam_step
+    for _ in range(max(args.warmup, 3)):
+        run(t)
+        t += 1
+    torch.cuda.synchronize()
+    n0 = muon.kernel_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        run(t)
+        t += 1
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"kernel": "adam", "bound": "hbm", "us_per_step": 1e3 * ms, "gbs": gbs,
+            "peak": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"], "bytes_per_step": nbytes,
+            "launches_per_step": (muon.kernel_launch_count() - n0) / args.steps,
+            "tensors": [f"{t.name}:{t.numel}" for t, *_ in sets],
+            "l2": "inputs larger than L2: %.0f MB moved per step" % (nbytes / 1e6)}
 
 
 def launches_per_step(step):

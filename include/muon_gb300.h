@@ -77,7 +77,8 @@ typedef enum muon_kernel_kind {
   MUON_K_GRAM = 2,       /* A = s^2 X X^T, upper tiles + mirror                 */
   MUON_K_POLY = 3,       /* B' = a I + b A + c A A, upper tiles + mirror        */
   MUON_K_UPDATE = 4,     /* X <- s B' X  (= s (a X + B X))                      */
-  MUON_K_APPLY = 5       /* p <- (1 - lr wd) p - lr scale O (or O as bf16)      */
+  MUON_K_APPLY = 5,      /* p <- (1 - lr wd) p - lr scale O (or O as bf16)      */
+  MUON_K_ADAM = 6        /* DistAdam update of non-matrix parameters            */
 } muon_kernel_kind;
 
 /* Workspace bytes for one muon_step()/muon_ns5() call on [batch, rows, cols].
@@ -164,6 +165,42 @@ muon_status muon_workspace_status(const void* workspace, size_t workspace_bytes,
  */
 muon_status muon_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int limit_us,
                                        void* stream);
+
+/*
+ * The Adam half of the optimizer: the DistAdam update that trains the
+ * parameters Muon does not take (embeddings, output head, {0,1}-D scalars).
+ * Defined by the DistAdam step() printed in "将 Adam 梯度同步（Reduce-Scatter）
+ * 移入反向 Hook：modded-nanogpt 分布式优化器每步提速约 0.7 秒的工程实践",
+ * section 改动二, with lr_eff = lr * lr_scale and t = `step`:
+ *   if weight_decay != 0:  p *= 1 - lr_eff * weight_decay * wd_scale
+ *   m = beta1 m + (1 - beta1) g;   v = beta2 v + (1 - beta2) g^2
+ *   p -= lr_eff * sqrt(1 - beta2^t) / (1 - beta1^t) * m / (sqrt(v) + eps)
+ * ([MCS] section 四 gives lr 0.008, betas (0.8, 0.95), eps 1e-8 for it.)
+ * On one GPU the reduce-scatter / all-gather of that page has no work: each
+ * tensor is updated whole, as one flat array of `numel` elements.
+ */
+typedef struct muon_adam_tensor {
+  float* param;         /* [numel] fp32, updated in place                        */
+  const void* grad;     /* [numel] in g_dtype, read only                         */
+  float* exp_avg;       /* [numel] fp32 first moment m, updated in place         */
+  float* exp_avg_sq;    /* [numel] fp32 second moment v, updated in place        */
+  long long numel;      /* >= 0; 0 skips the tensor (its pointers may be NULL)   */
+  int g_dtype;          /* muon_dtype of grad                                    */
+  float lr_scale;       /* per-parameter lr multiplier (1 = none), finite, >= 0  */
+  float wd_scale;       /* per-parameter weight-decay multiplier (1 = none)      */
+} muon_adam_tensor;
+
+/*
+ * One Adam step over n_tensors >= 0 tensors (tensors may be NULL only when
+ * n_tensors == 0), all at step count `step` >= 1 (the value after the
+ * increment).  0 <= beta1, beta2 < 1; eps >= 0; lr and weight_decay finite.
+ * Pointers 16-byte aligned; the arrays of different tensors must not overlap.
+ * Up to 64 tensors go in one kernel launch; more take one launch per 64.
+ * Needs no workspace and has no waits.
+ */
+muon_status muon_adam_step(const muon_adam_tensor* tensors, int n_tensors, int step, float lr,
+                           float beta1, float beta2, float eps, float weight_decay,
+                           void* stream);
 
 /* Static English text for a status code. */
 const char* muon_status_string(muon_status status);

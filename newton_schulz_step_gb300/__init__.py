@@ -10,6 +10,7 @@ Entry points mirror the C ABI:
   ns5(G)                         zeropower_via_newtonschulz5 on a stack of matrices
   step(p, g, buf, ...)           one Muon step on a stack of same-shape weights
   step_grouped([(p, g, buf)...]) one Muon step on every group of a model
+  adam_step([(p, g, m, v)...])   one DistAdam step on the non-matrix parameters
 """
 
 from __future__ import annotations
@@ -22,7 +23,7 @@ import torch
 __all__ = [
     "COEFFS", "EPS", "MuonError", "load_library", "library_path", "workspace_bytes",
     "grouped_workspace_bytes", "Workspace", "ns5", "step", "step_noalloc", "step_grouped",
-    "GroupedStep",
+    "GroupedStep", "AdamStep", "adam_step", "ADAM_LR", "ADAM_BETAS", "ADAM_EPS",
     "workspace_status", "status_string", "kernel_launch_count", "trace_begin", "trace_end",
     "KERNEL_KINDS",
 ]
@@ -32,7 +33,13 @@ COEFFS = (3.4445, -4.7750, 2.0315)
 STEPS = 5
 EPS = 1e-7
 
-KERNEL_KINDS = {0: "prologue", 1: "small_ns", 2: "gram", 3: "poly", 4: "update", 5: "apply"}
+# DistAdam settings printed in "Muon Custom Sizing 实战", section 四.
+ADAM_LR = 0.008
+ADAM_BETAS = (0.8, 0.95)
+ADAM_EPS = 1e-8
+
+KERNEL_KINDS = {0: "prologue", 1: "small_ns", 2: "gram", 3: "poly", 4: "update", 5: "apply",
+                6: "adam"}
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "timeout",
            5: "workspace"}
 
@@ -55,6 +62,13 @@ class _Group(ctypes.Structure):
                 ("momentum_buf", ctypes.c_void_p), ("g_dtype", ctypes.c_int),
                 ("batch", ctypes.c_int), ("rows", ctypes.c_int), ("cols", ctypes.c_int),
                 ("lr_scale", ctypes.c_float)]
+
+
+class _AdamTensor(ctypes.Structure):
+    _fields_ = [("param", ctypes.c_void_p), ("grad", ctypes.c_void_p),
+                ("exp_avg", ctypes.c_void_p), ("exp_avg_sq", ctypes.c_void_p),
+                ("numel", ctypes.c_longlong), ("g_dtype", ctypes.c_int),
+                ("lr_scale", ctypes.c_float), ("wd_scale", ctypes.c_float)]
 
 
 class _TraceRecord(ctypes.Structure):
@@ -91,6 +105,8 @@ def load_library():
     L.muon_workspace_status.restype = ci
     L.muon_selftest_wait_timeout.argtypes = [vp, sz, ci, vp]
     L.muon_selftest_wait_timeout.restype = ci
+    L.muon_adam_step.argtypes = [ctypes.POINTER(_AdamTensor), ci, ci, cf, cf, cf, cf, cf, vp]
+    L.muon_adam_step.restype = ci
     L.muon_status_string.argtypes = [ci]
     L.muon_status_string.restype = ctypes.c_char_p
     L.muon_kernel_launch_count.argtypes = []
@@ -313,6 +329,49 @@ def step_grouped(groups, *, momentum: float, lr: float, weight_decay: float,
     """One Muon step over every group: groups = [(params, grads, bufs[, lr_scale]), ...]."""
     GroupedStep(groups, momentum=momentum, lr=lr, weight_decay=weight_decay, nesterov=nesterov,
                 steps=steps, coeffs=coeffs, eps=eps, workspace=workspace)(stream)
+
+
+class AdamStep:
+    """A prepared muon_adam_step call over tensors = [(param, grad, exp_avg, exp_avg_sq
+    [, lr_scale[, wd_scale]]), ...]; param and the moments are fp32, grad fp32 or bf16,
+    all contiguous CUDA tensors of one numel per entry (any shape).  Calling it with
+    the step count t (>= 1, after the increment) enqueues one update."""
+
+    def __init__(self, tensors, *, lr: float = ADAM_LR, betas=ADAM_BETAS, eps: float = ADAM_EPS,
+                 weight_decay: float = 0.0):
+        load_library()
+        self._keep = []
+        self._arr = (_AdamTensor * max(1, len(tensors)))()
+        for i, ent in enumerate(tensors):
+            p, g, m, v = ent[:4]
+            ls = float(ent[4]) if len(ent) > 4 else 1.0
+            ws = float(ent[5]) if len(ent) > 5 else 1.0
+            for t, name in ((p, "param"), (g, "grad"), (m, "exp_avg"), (v, "exp_avg_sq")):
+                if not t.is_cuda or not t.is_contiguous():
+                    raise ValueError(f"{name} must be a contiguous CUDA tensor")
+            if p.dtype != torch.float32 or m.dtype != torch.float32 or v.dtype != torch.float32:
+                raise TypeError("param, exp_avg and exp_avg_sq must be float32")
+            if not (p.numel() == g.numel() == m.numel() == v.numel()):
+                raise ValueError("param, grad, exp_avg and exp_avg_sq must have the same numel")
+            a = self._arr[i]
+            a.param, a.grad, a.exp_avg, a.exp_avg_sq = (t.data_ptr() for t in (p, g, m, v))
+            a.numel, a.g_dtype, a.lr_scale, a.wd_scale = p.numel(), _gdt(g), ls, ws
+            self._keep.append((p, g, m, v))
+        self._n = len(tensors)
+        self._scalars = (float(lr), float(betas[0]), float(betas[1]), float(eps),
+                         float(weight_decay))
+
+    def __call__(self, step: int, stream=None):
+        lr, b1, b2, eps, wd = self._scalars
+        _raise(load_library().muon_adam_step(self._arr, self._n, int(step), lr, b1, b2, eps, wd,
+                                             _stream_handle(stream)), "muon_adam_step")
+
+
+def adam_step(tensors, step: int, *, lr: float = ADAM_LR, betas=ADAM_BETAS, eps: float = ADAM_EPS,
+              weight_decay: float = 0.0, stream=None):
+    """One DistAdam update, in place, of every (param, grad, exp_avg, exp_avg_sq[, lr_scale
+    [, wd_scale]]) entry at step count `step` (>= 1)."""
+    AdamStep(tensors, lr=lr, betas=betas, eps=eps, weight_decay=weight_decay)(step, stream)
 
 
 def workspace_status(workspace: Workspace, clear: bool = False, stream=None) -> int:

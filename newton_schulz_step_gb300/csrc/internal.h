@@ -126,6 +126,29 @@ struct GemmLaunch {
 
 enum GemmStage : int { kStageGram = 0, kStagePoly = 1, kStageUpdate = 2 };
 
+// ---- DistAdam update (adam.cu)
+constexpr int kAdamUnit = 4096;       // elements per work unit (256 threads x 4 float4)
+constexpr int kMaxAdamTensors = 64;   // tensors per launch
+
+struct AdamTensor {
+  float* p;
+  const void* g;
+  float* m;
+  float* v;
+  long long n;           // elements
+  long long unit_begin;  // first unit of this tensor in the launch
+  float step_size;       // lr_eff * sqrt(1 - b2^t) / (1 - b1^t)
+  float decay;           // 1 - lr_eff * wd * wd_scale (1 when wd == 0)
+  int g_bf16;
+};
+
+struct AdamLaunch {
+  AdamTensor t[kMaxAdamTensors];
+  int n_tensors;
+  long long total_units;
+  float beta1, beta2, eps;
+};
+
 // Launchers (defined next to their kernels).  Each returns a cudaError_t from
 // the launch; grid sizes come from the caller's SM count.
 // The prologue may be launched as a programmatic dependent of the kernel
@@ -140,5 +163,7 @@ cudaError_t launch_gemm(const GemmLaunch& l, int stage, int pair_tiles, int sms,
 int gemm_smem_bytes();
 cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_ns,
                                  cudaStream_t s);
+cudaError_t launch_adam(const AdamLaunch& l, int blocks, cudaStream_t s);
+int adam_blocks_per_sm();  // resident Adam blocks per SM on the current device (0 on error)
 
 }  // namespace muon

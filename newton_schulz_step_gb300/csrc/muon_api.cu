@@ -645,6 +645,84 @@ muon_status muon_selftest_wait_timeout(void* workspace, size_t workspace_bytes, 
   return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
 }
 
+muon_status muon_adam_step(const muon_adam_tensor* tensors, int n_tensors, int step, float lr,
+                           float beta1, float beta2, float eps, float weight_decay,
+                           void* stream) {
+  try {
+    if (n_tensors < 0 || (n_tensors > 0 && !tensors) || step < 1) return MUON_ERR_INVALID_ARG;
+    if (!(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f) ||
+        !(eps >= 0.f && std::isfinite(eps)) || !std::isfinite(lr) ||
+        !std::isfinite(weight_decay))
+      return MUON_ERR_INVALID_ARG;
+    long long work = 0;
+    for (int i = 0; i < n_tensors; ++i) {
+      const muon_adam_tensor& t = tensors[i];
+      if (t.numel < 0) return MUON_ERR_INVALID_ARG;
+      if (t.numel == 0) continue;
+      work += t.numel;
+      if (t.g_dtype != MUON_F32 && t.g_dtype != MUON_BF16) return MUON_ERR_INVALID_ARG;
+      if (!t.param || !t.grad || !t.exp_avg || !t.exp_avg_sq || !aligned16(t.param) ||
+          !aligned16(t.grad) || !aligned16(t.exp_avg) || !aligned16(t.exp_avg_sq))
+        return MUON_ERR_INVALID_ARG;
+      if (!(t.lr_scale >= 0.f && std::isfinite(t.lr_scale)) || !std::isfinite(t.wd_scale))
+        return MUON_ERR_INVALID_ARG;
+    }
+    if (work == 0) return MUON_OK;  // nothing to update: nothing is enqueued
+    int sms = 0;
+    const muon_status ds = current_device(&sms);
+    if (ds != MUON_OK) return ds;
+    const int per_sm = adam_blocks_per_sm();
+    if (per_sm < 1) return MUON_ERR_CUDA;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // bias corrections in double, as the page computes them in Python floats
+    const double bias1 = 1.0 - std::pow(static_cast<double>(beta1), step);
+    const double bias2 = 1.0 - std::pow(static_cast<double>(beta2), step);
+    AdamLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    L.beta1 = beta1;
+    L.beta2 = beta2;
+    L.eps = eps;
+    double bytes = 0.0;
+    auto flush = [&]() -> muon_status {
+      if (L.n_tensors == 0) return MUON_OK;
+      const long long blocks = std::min<long long>(L.total_units, 1ll * sms * per_sm);
+      const cudaError_t e = tracked_launch(st, {MUON_K_ADAM, -1, 0.0, bytes}, [&] {
+        return launch_adam(L, static_cast<int>(blocks), st);
+      });
+      L.n_tensors = 0;
+      L.total_units = 0;
+      bytes = 0.0;
+      return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+    };
+    for (int i = 0; i < n_tensors; ++i) {
+      const muon_adam_tensor& t = tensors[i];
+      if (t.numel == 0) continue;
+      const double lr_eff = static_cast<double>(lr) * t.lr_scale;
+      AdamTensor& a = L.t[L.n_tensors++];
+      a.p = t.param;
+      a.g = t.grad;
+      a.m = t.exp_avg;
+      a.v = t.exp_avg_sq;
+      a.n = t.numel;
+      a.unit_begin = L.total_units;
+      a.step_size = static_cast<float>(lr_eff * (std::sqrt(bias2) / bias1));
+      a.decay = weight_decay != 0.f
+                    ? static_cast<float>(1.0 - lr_eff * weight_decay * t.wd_scale)
+                    : 1.f;
+      a.g_bf16 = t.g_dtype == MUON_BF16;
+      L.total_units += (t.numel + kAdamUnit - 1) / kAdamUnit;
+      bytes += static_cast<double>(t.numel) * (24 + (a.g_bf16 ? 2 : 4));
+      if (L.n_tensors == kMaxAdamTensors) {
+        const muon_status fs = flush();
+        if (fs != MUON_OK) return fs;
+      }
+    }
+    return flush();
+  } catch (...) {
+    return MUON_ERR_CUDA;
+  }
+}
+
 const char* muon_status_string(muon_status status) {
   switch (status) {
     case MUON_OK:

@@ -138,3 +138,45 @@ def test_well_formed_call_without_gpu_is_refused(lib):
     assert code in (UNSUPPORTED, CUDA)
     with pytest.raises(Exception):
         muon.ns5(torch.zeros(4, 64, 64))   # CPU tensor: the binding refuses as well
+
+
+def _adam_arr(n=1, numel=1000, ptr=0x10000, dtype=1):
+    arr = (muon._AdamTensor * max(1, n))()
+    for i in range(n):
+        a = arr[i]
+        a.param, a.grad, a.exp_avg, a.exp_avg_sq = ptr, ptr + 0x100000, ptr + 0x200000, ptr + 0x300000
+        a.numel, a.g_dtype, a.lr_scale, a.wd_scale = numel, dtype, 1.0, 1.0
+    return arr
+
+
+def test_adam_argument_errors(lib):
+    f = lib.muon_adam_step
+    arr = _adam_arr()
+    assert f(arr, -1, 1, 0.008, 0.8, 0.95, 1e-8, 0.0, None) == INVALID
+    assert f(None, 1, 1, 0.008, 0.8, 0.95, 1e-8, 0.0, None) == INVALID
+    assert f(arr, 1, 0, 0.008, 0.8, 0.95, 1e-8, 0.0, None) == INVALID        # step counts from 1
+    assert f(arr, 1, 1, 0.008, 1.0, 0.95, 1e-8, 0.0, None) == INVALID        # beta1 < 1
+    assert f(arr, 1, 1, 0.008, 0.8, -0.1, 1e-8, 0.0, None) == INVALID        # beta2 >= 0
+    assert f(arr, 1, 1, 0.008, 0.8, 0.95, -1e-8, 0.0, None) == INVALID       # eps >= 0
+    assert f(arr, 1, 1, float("nan"), 0.8, 0.95, 1e-8, 0.0, None) == INVALID
+    assert f(arr, 1, 1, 0.008, 0.8, 0.95, 1e-8, float("inf"), None) == INVALID
+    assert f(_adam_arr(ptr=0x10008), 1, 1, 0.008, 0.8, 0.95, 1e-8, 0.0, None) == INVALID
+    assert f(_adam_arr(dtype=7), 1, 1, 0.008, 0.8, 0.95, 1e-8, 0.0, None) == INVALID
+    assert f(_adam_arr(numel=-5), 1, 1, 0.008, 0.8, 0.95, 1e-8, 0.0, None) == INVALID
+    bad = _adam_arr()
+    bad[0].grad = None
+    assert f(bad, 1, 1, 0.008, 0.8, 0.95, 1e-8, 0.0, None) == INVALID
+    bad = _adam_arr()
+    bad[0].lr_scale = -1.0
+    assert f(bad, 1, 1, 0.008, 0.8, 0.95, 1e-8, 0.0, None) == INVALID
+    # nothing to do is OK without touching a device
+    assert f(None, 0, 1, 0.008, 0.8, 0.95, 1e-8, 0.0, None) == OK
+    empty = _adam_arr(numel=0)
+    empty[0].param = empty[0].grad = empty[0].exp_avg = empty[0].exp_avg_sq = None
+    assert f(empty, 1, 1, 0.008, 0.8, 0.95, 1e-8, 0.0, None) == OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU refusal")
+def test_adam_without_gpu_is_refused(lib):
+    code = lib.muon_adam_step(_adam_arr(), 1, 1, 0.008, 0.8, 0.95, 1e-8, 0.0, None)
+    assert code in (UNSUPPORTED, CUDA)

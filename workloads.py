@@ -19,6 +19,13 @@ Shapes follow the GPT models the pages train: the d=768 GPT-2 124M stack of
 the modded-nanogpt record, whose attention weight is stored as (hdim, 4*dim)
 and viewed as four (hdim, dim) blocks (Q, K, V, O) before orthogonalisation,
 and the 9-layer d=512 model of parameter-golf.
+
+The Adam half of the optimizer takes the parameters Muon does not: for the
+GPT-2 124M stack the token embedding and the output head (vocab 50257 x 768
+each, the sizes of that page's model) and a small vector of scalars (64
+entries: the count is not printed).  Their seeds are
+  seed(tensor i, kind k) = workload.seed * 10_000_000 + 5_000_000 + 4 * i + k
+  k = 0 gradient, 1 parameter, 2 exp_avg, 3 exp_avg_sq.
 """
 
 from __future__ import annotations
@@ -48,6 +55,19 @@ class Group:
 
 
 @dataclass(frozen=True)
+class AdamTensor:
+    """One parameter trained by the Adam half of the optimizer (flat, any shape)."""
+    name: str
+    shape: tuple
+    lr_scale: float = 1.0
+    wd_scale: float = 1.0
+
+    @property
+    def numel(self):
+        return math.prod(self.shape)
+
+
+@dataclass(frozen=True)
 class Workload:
     name: str
     description: str
@@ -64,6 +84,12 @@ class Workload:
     heavy_row_scale: float = 100.0
     steps: int = 5
     nesterov: bool = True
+    adam: tuple = ()          # AdamTensor entries: embeddings, head, scalars
+    adam_step: int = 100      # Adam step count t of the drawn state
+
+    @property
+    def adam_numel(self):
+        return sum(t.numel for t in self.adam)
 
     @property
     def n_matrices(self):
@@ -97,7 +123,9 @@ _W = [
         groups=(Group("smear_gate", 1, 1, 12), Group("attn_gate", 10, 12, 768),
                 Group("attn_qkvo", 40, 768, 768, stored=(10, 768, 3072)),
                 Group("mlp_fc", 11, 768, 3072), Group("mlp_proj", 11, 3072, 768)),
-        grad_dtype=torch.bfloat16, grad_std=1e-3, momentum=0.95),
+        grad_dtype=torch.bfloat16, grad_std=1e-3, momentum=0.95,
+        adam=(AdamTensor("embed", (50257, 768)), AdamTensor("lm_head", (50257, 768)),
+              AdamTensor("scalars", (64,)))),
     Workload(
         name="gpt-24L-d2048",
         description="24-layer d=2048 GPT: 96 attn 2048x2048, 24 MLP-up 8192x2048, 24 MLP-down "
@@ -186,6 +214,32 @@ def make_group(wl: Workload, group_index: int, device="cpu"):
 def make_workload(wl: Workload, device="cpu"):
     """List of (Group, params, grads, bufs) for every group of the workload."""
     return [(grp, *make_group(wl, gi, device)) for gi, grp in enumerate(wl.groups)]
+
+
+def adam_seed(wl: Workload, tensor_index: int, kind: int) -> int:
+    return wl.seed * 10_000_000 + 5_000_000 + 4 * tensor_index + kind
+
+
+def draw_adam_tensor(wl: Workload, index: int, device="cpu", spec: AdamTensor | None = None):
+    """(param fp32, grad, exp_avg fp32, exp_avg_sq fp32) of one Adam tensor, flat.
+
+    Mid-training state: grad ~ N(0, grad_std) in the workload's gradient dtype,
+    param ~ N(0, param_std), exp_avg ~ N(0, grad_std), exp_avg_sq = N(0, grad_std)^2.
+    """
+    spec = spec or wl.adam[index]
+    n = spec.numel
+    g = (torch.randn(n, generator=_gen(device, adam_seed(wl, index, 0)), device=device)
+         * wl.grad_std).to(wl.grad_dtype)
+    p = torch.randn(n, generator=_gen(device, adam_seed(wl, index, 1)), device=device) * wl.param_std
+    m = torch.randn(n, generator=_gen(device, adam_seed(wl, index, 2)), device=device) * wl.grad_std
+    v = (torch.randn(n, generator=_gen(device, adam_seed(wl, index, 3)), device=device)
+         * wl.grad_std) ** 2
+    return p, g, m, v
+
+
+def make_adam_set(wl: Workload, device="cpu"):
+    """List of (AdamTensor, param, grad, exp_avg, exp_avg_sq) of the workload."""
+    return [(t, *draw_adam_tensor(wl, i, device)) for i, t in enumerate(wl.adam)]
 
 
 def sample_indices(batch: int):
