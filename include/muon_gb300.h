@@ -78,7 +78,9 @@ typedef enum muon_kernel_kind {
   MUON_K_POLY = 3,       /* B' = a I + b A + c A A, upper tiles + mirror        */
   MUON_K_UPDATE = 4,     /* X <- s B' X  (= s (a X + B X))                      */
   MUON_K_APPLY = 5,      /* p <- (1 - lr wd) p - lr scale O (or O as bf16)      */
-  MUON_K_ADAM = 6        /* DistAdam update of non-matrix parameters            */
+  MUON_K_ADAM = 6,       /* DistAdam update of non-matrix parameters            */
+  MUON_K_FUSED_NS = 7    /* whole step, one CTA pair per matrix, 64<=m<=256,
+                            n<=512 (see muon_set_fused_ns)                      */
 } muon_kernel_kind;
 
 /* Workspace bytes for one muon_step()/muon_ns5() call on [batch, rows, cols].
@@ -201,6 +203,19 @@ typedef struct muon_adam_tensor {
 muon_status muon_adam_step(const muon_adam_tensor* tensors, int n_tensors, int step, float lr,
                            float beta1, float beta2, float eps, float weight_decay,
                            void* stream);
+
+/*
+ * Path selection (no counterpart on the pages).  With enable = 1 (the default)
+ * every matrix with 64 <= min(rows, cols) <= 256 and max(rows, cols) <= 512
+ * runs its whole step -- momentum, NS rounds, parameter write -- in one kernel,
+ * one CTA pair per matrix, with X, A and B' held on chip; enable = 0 sends it
+ * through the staged tensor-core path (a prologue, three GEMM stages per round
+ * and an apply, with X, A and B' in the workspace).  Both compute the same step
+ * and need the same workspace size.  Process-wide; affects calls made
+ * afterwards.  Returns the previous setting, or -1 (nothing changed) if
+ * enable is not 0 or 1.
+ */
+int muon_set_fused_ns(int enable);
 
 /* Static English text for a status code. */
 const char* muon_status_string(muon_status status);

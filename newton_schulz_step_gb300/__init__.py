@@ -25,6 +25,7 @@ __all__ = [
     "grouped_workspace_bytes", "Workspace", "ns5", "step", "step_noalloc", "step_grouped",
     "GroupedStep", "AdamStep", "adam_step", "ADAM_LR", "ADAM_BETAS", "ADAM_EPS",
     "workspace_status", "status_string", "kernel_launch_count", "trace_begin", "trace_end",
+    "set_fused_ns", "fused_ns",
     "KERNEL_KINDS",
 ]
 
@@ -39,7 +40,7 @@ ADAM_BETAS = (0.8, 0.95)
 ADAM_EPS = 1e-8
 
 KERNEL_KINDS = {0: "prologue", 1: "small_ns", 2: "gram", 3: "poly", 4: "update", 5: "apply",
-                6: "adam"}
+                6: "adam", 7: "fused_ns"}
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "timeout",
            5: "workspace"}
 
@@ -107,6 +108,8 @@ def load_library():
     L.muon_selftest_wait_timeout.restype = ci
     L.muon_adam_step.argtypes = [ctypes.POINTER(_AdamTensor), ci, ci, cf, cf, cf, cf, cf, vp]
     L.muon_adam_step.restype = ci
+    L.muon_set_fused_ns.argtypes = [ci]
+    L.muon_set_fused_ns.restype = ci
     L.muon_status_string.argtypes = [ci]
     L.muon_status_string.restype = ctypes.c_char_p
     L.muon_kernel_launch_count.argtypes = []
@@ -385,6 +388,31 @@ def selftest_wait_timeout(workspace: Workspace, limit_us: int = 1000, stream=Non
     _raise(load_library().muon_selftest_wait_timeout(workspace.ptr, workspace.nbytes, limit_us,
                                                      _stream_handle(stream)),
            "muon_selftest_wait_timeout")
+
+
+def set_fused_ns(enable: bool) -> bool:
+    """Route 64 <= min(r, c) <= 256, max(r, c) <= 512 matrices through the one-kernel
+    fused path (True, the default) or the staged path (False); returns the previous value."""
+    prev = int(load_library().muon_set_fused_ns(int(bool(enable))))
+    if prev < 0:
+        raise MuonError(1, "muon_set_fused_ns")
+    return bool(prev)
+
+
+class fused_ns:
+    """Context manager: `with fused_ns(False): ...` runs the block on the staged path."""
+
+    def __init__(self, enable: bool):
+        self.enable = bool(enable)
+        self.prev = None
+
+    def __enter__(self):
+        self.prev = set_fused_ns(self.enable)
+        return self
+
+    def __exit__(self, *exc):
+        set_fused_ns(self.prev)
+        return False
 
 
 def kernel_launch_count() -> int:

@@ -26,6 +26,7 @@ enum DeviceError : unsigned int {
   kErrTimeoutMma = 2u,
   kErrTimeoutEpilogue = 4u,
   kErrTimeoutDrain = 8u,
+  kErrTimeoutFused = 16u,
 };
 
 // What the prologue computes from (g, buf).
@@ -126,6 +127,32 @@ struct GemmLaunch {
 
 enum GemmStage : int { kStageGram = 0, kStagePoly = 1, kStageUpdate = 2 };
 
+// ---- fused whole-step kernel for 64 <= m <= 256, n <= 512 (ns_fused.cu)
+constexpr int kFusedMaxM = 256;
+constexpr int kFusedMaxN = 512;
+constexpr int kMaxFusedGroups = 16;
+
+struct FusedGroup {
+  const void* g;
+  float* buf;
+  float* param;
+  __nv_bfloat16* out;   // NS-only mode: bf16 result [batch, r, c]
+  int gdt;
+  int batch, r, c;
+  int cluster_begin;    // first CTA pair of this group in the launch
+  float lr_eff;         // lr * rescale
+};
+
+struct FusedLaunch {
+  FusedGroup grp[kMaxFusedGroups];
+  int n_groups;
+  int total_clusters;
+  int mode;             // PrologueMode
+  int steps;
+  float beta, a, b, c, eps, decay;
+  unsigned int* status;
+};
+
 // ---- DistAdam update (adam.cu)
 constexpr int kAdamUnit = 4096;       // elements per work unit (256 threads x 4 float4)
 constexpr int kMaxAdamTensors = 64;   // tensors per launch
@@ -164,6 +191,10 @@ int gemm_smem_bytes();
 cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_ns,
                                  cudaStream_t s);
 cudaError_t launch_adam(const AdamLaunch& l, int blocks, cudaStream_t s);
+// One CTA pair per matrix of every group in `l`; pdl = launched as a
+// programmatic dependent of the kernel before it (it then waits for that
+// kernel only before exiting).
+cudaError_t launch_fused(const FusedLaunch& l, bool pdl, cudaStream_t s);
 int adam_blocks_per_sm();  // resident Adam blocks per SM on the current device (0 on error)
 
 }  // namespace muon

@@ -27,6 +27,8 @@ namespace {
 
 // ------------------------------------------------------------ bookkeeping
 std::atomic<unsigned long long> g_launch_count{0};
+// 1: matrices with 64 <= m <= 256 and n <= 512 take the one-kernel fused path
+std::atomic<int> g_fused_enabled{1};
 
 struct TraceSlot {
   cudaEvent_t e0 = nullptr, e1 = nullptr;
@@ -424,10 +426,72 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
     if (s != MUON_OK) return s;
   }
 
+  // -- matrices with 64 <= m <= 256 and n <= 512: the whole step in one kernel
+  //    (one CTA pair per matrix), a programmatic dependent of the kernel before
+  //    so that it runs beside it
+  const bool fuse = g_fused_enabled.load(std::memory_order_relaxed) != 0;
+  auto is_fused = [&](const GPlan& g) {
+    return fuse && !g.small && g.m <= kFusedMaxM && g.n <= kFusedMaxN;
+  };
+  bool fused_launched = false;
+  {
+    FusedLaunch fl;
+    std::memset(&fl, 0, sizeof(fl));
+    fl.mode = sc.mode;
+    fl.steps = sc.steps;
+    fl.beta = sc.beta;
+    fl.a = sc.a;
+    fl.b = sc.b;
+    fl.c = sc.c;
+    fl.eps = sc.eps;
+    fl.decay = 1.0f - sc.lr * sc.wd;
+    fl.status = reinterpret_cast<unsigned int*>(ws);
+    double flops = 0, bytes = 0;
+    auto flush = [&]() -> muon_status {
+      if (fl.n_groups == 0) return MUON_OK;
+      const bool pdl = small_launched || fused_launched;
+      const cudaError_t e = tracked_launch(st, {MUON_K_FUSED_NS, -1, flops, bytes},
+                                           [&] { return launch_fused(fl, pdl, st); });
+      fl.n_groups = 0;
+      fl.total_clusters = 0;
+      flops = bytes = 0;
+      fused_launched = true;
+      return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+    };
+    for (GPlan& g : gs) {
+      if (!is_fused(g) || g.batch == 0) continue;
+      FusedGroup& fg = fl.grp[fl.n_groups++];
+      fg.g = g.g;
+      fg.buf = g.buf;
+      fg.param = g.p;
+      fg.out = g.out;
+      fg.gdt = g.gdt;
+      fg.batch = g.batch;
+      fg.r = g.r;
+      fg.c = g.c;
+      fg.cluster_begin = fl.total_clusters;
+      const float scale = g.lr_scale > 0.f ? g.lr_scale
+                                            : static_cast<float>(std::sqrt(std::max(
+                                                  1.0, static_cast<double>(g.r) / g.c)));
+      fg.lr_eff = sc.lr * scale;
+      fl.total_clusters += g.batch;
+      const double mm = g.m, nn = g.n;
+      flops += static_cast<double>(g.batch) * sc.steps * (4.0 * mm * mm * nn + 2.0 * mm * mm * mm);
+      bytes += static_cast<double>(g.batch) * g.r * g.c *
+               ((g.gdt == MUON_BF16 ? 2.0 : 4.0) + (sc.mode == kPrologueNsOnly ? 2.0 : 16.0));
+      if (fl.n_groups == kMaxFusedGroups) {
+        s = flush();
+        if (s != MUON_OK) return s;
+      }
+    }
+    s = flush();
+    if (s != MUON_OK) return s;
+  }
+
   // -- tensor-core matrices: one grouped prologue launch (per kMaxPrologueGroups)
   std::vector<GPlan*> big;
   for (GPlan& g : gs)
-    if (!g.small && g.batch > 0) big.push_back(&g);
+    if (!g.small && !is_fused(g) && g.batch > 0) big.push_back(&g);
   for (size_t c0 = 0; c0 < big.size(); c0 += kMaxPrologueGroups) {
     PrologueLaunch pl;
     std::memset(&pl, 0, sizeof(pl));
@@ -453,7 +517,7 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
                ((g.gdt == MUON_BF16 ? 2.0 : 4.0) + 2.0 + (sc.mode == kPrologueNsOnly ? 0.0 : 8.0));
     }
     pl.total_blocks = blocks;
-    const bool pdl = small_launched && c0 == 0;
+    const bool pdl = (small_launched || fused_launched) && c0 == 0;
     pl.wait_prior = pdl ? 1 : 0;
     const cudaError_t e = tracked_launch(st, {MUON_K_PROLOGUE, -1, 0.0, bytes},
                                          [&] { return launch_prologue(pl, sc.mode, pdl, st); });
@@ -739,6 +803,11 @@ const char* muon_status_string(muon_status status) {
       return "workspace missing, misaligned or too small";
   }
   return "unknown status";
+}
+
+int muon_set_fused_ns(int enable) {
+  if (enable != 0 && enable != 1) return -1;
+  return g_fused_enabled.exchange(enable);
 }
 
 unsigned long long muon_kernel_launch_count(void) {
