@@ -79,7 +79,7 @@ typedef enum muon_kernel_kind {
   MUON_K_UPDATE = 4,     /* X <- s B' X  (= s (a X + B X))                      */
   MUON_K_APPLY = 5,      /* p <- (1 - lr wd) p - lr scale O (or O as bf16)      */
   MUON_K_ADAM = 6,       /* DistAdam update of non-matrix parameters            */
-  MUON_K_FUSED_NS = 7    /* whole step, one CTA pair per matrix, 64<=m<=256,
+  MUON_K_FUSED_NS = 7    /* all NS rounds, one CTA pair per matrix, 64<=m<=256,
                             n<=512 (see muon_set_fused_ns)                      */
 } muon_kernel_kind;
 
@@ -207,13 +207,16 @@ muon_status muon_adam_step(const muon_adam_tensor* tensors, int n_tensors, int s
 /*
  * Path selection (no counterpart on the pages).  With enable = 1 (the default)
  * every matrix with 64 <= min(rows, cols) <= 256 and max(rows, cols) <= 512
- * runs its whole step -- momentum, NS rounds, parameter write -- in one kernel,
- * one CTA pair per matrix, with X, A and B' held on chip; enable = 0 sends it
- * through the staged tensor-core path (a prologue, three GEMM stages per round
- * and an apply, with X, A and B' in the workspace).  Both compute the same step
- * and need the same workspace size.  Process-wide; affects calls made
- * afterwards.  Returns the previous setting, or -1 (nothing changed) if
- * enable is not 0 or 1.
+ * runs all its NS rounds in one kernel, one CTA pair per matrix, with X, A and
+ * B' held on chip between rounds; enable = 0 sends it through the staged
+ * tensor-core path (three GEMM launches per round, with A and B' in the
+ * workspace).  The grouped prologue and apply are the same on both paths.
+ * A call that also holds matrices outside that range (which need the staged
+ * launches) runs all of them staged, since the fused kernel would run before
+ * the staged chain rather than beside it.
+ * Both compute the same step and need the same workspace size.  Process-wide;
+ * affects calls made afterwards.  Returns the previous setting, or -1 (nothing
+ * changed) if enable is not 0 or 1.
  */
 int muon_set_fused_ns(int enable);
 

@@ -391,8 +391,9 @@ def selftest_wait_timeout(workspace: Workspace, limit_us: int = 1000, stream=Non
 
 
 def set_fused_ns(enable: bool) -> bool:
-    """Route 64 <= min(r, c) <= 256, max(r, c) <= 512 matrices through the one-kernel
-    fused path (True, the default) or the staged path (False); returns the previous value."""
+    """Run the NS rounds of 64 <= min(r, c) <= 256, max(r, c) <= 512 matrices in one fused
+    kernel (True, the default) or in the staged GEMM launches (False); returns the previous
+    value."""
     prev = int(load_library().muon_set_fused_ns(int(bool(enable))))
     if prev < 0:
         raise MuonError(1, "muon_set_fused_ns")

@@ -127,29 +127,30 @@ struct GemmLaunch {
 
 enum GemmStage : int { kStageGram = 0, kStagePoly = 1, kStageUpdate = 2 };
 
-// ---- fused whole-step kernel for 64 <= m <= 256, n <= 512 (ns_fused.cu)
+// ---- fused NS kernel for 64 <= m <= 256, n <= 512 (ns_fused.cu): all rounds
+// of one matrix on one CTA pair; X0 and the norm partials come from the
+// grouped prologue, the result O goes where the staged path leaves it
 constexpr int kFusedMaxM = 256;
 constexpr int kFusedMaxN = 512;
 constexpr int kMaxFusedGroups = 16;
 
 struct FusedGroup {
-  const void* g;
-  float* buf;
-  float* param;
-  __nv_bfloat16* out;   // NS-only mode: bf16 result [batch, r, c]
-  int gdt;
-  int batch, r, c;
-  int cluster_begin;    // first CTA pair of this group in the launch
-  float lr_eff;         // lr * rescale
+  const float* parts;   // [batch, nparts] partial sums of u^2
+  int nparts;
+  int batch, m, n;
+  int cluster_begin;    // first matrix (CTA pair, or CTA) of this group in the launch
 };
 
 struct FusedLaunch {
+  // bf16 [batch][m][ldx] X buffers 0 and 1 (SW128, 64 x 128 boxes): round it
+  // reads buffer it & 1 and writes buffer (it + 1) & 1
+  CUtensorMap tm_x[kMaxFusedGroups][2];
   FusedGroup grp[kMaxFusedGroups];
   int n_groups;
-  int total_clusters;
-  int mode;             // PrologueMode
+  int total_clusters;   // matrices in the launch
+  int pair;             // 1: a CTA pair per matrix (m <= 256); 0: one CTA (m <= 128)
   int steps;
-  float beta, a, b, c, eps, decay;
+  float a, b, c, eps;
   unsigned int* status;
 };
 
@@ -191,10 +192,10 @@ int gemm_smem_bytes();
 cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_ns,
                                  cudaStream_t s);
 cudaError_t launch_adam(const AdamLaunch& l, int blocks, cudaStream_t s);
-// One CTA pair per matrix of every group in `l`; pdl = launched as a
-// programmatic dependent of the kernel before it (it then waits for that
-// kernel only before exiting).
-cudaError_t launch_fused(const FusedLaunch& l, bool pdl, cudaStream_t s);
+// One CTA pair (l.pair) or one CTA per matrix of every group in `l`, launched as a programmatic
+// dependent of the kernel before it (the prologue), whose output it reads
+// after griddepcontrol.wait.
+cudaError_t launch_fused(const FusedLaunch& l, cudaStream_t s);
 int adam_blocks_per_sm();  // resident Adam blocks per SM on the current device (0 on error)
 
 }  // namespace muon

@@ -426,72 +426,23 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
     if (s != MUON_OK) return s;
   }
 
-  // -- matrices with 64 <= m <= 256 and n <= 512: the whole step in one kernel
-  //    (one CTA pair per matrix), a programmatic dependent of the kernel before
-  //    so that it runs beside it
-  const bool fuse = g_fused_enabled.load(std::memory_order_relaxed) != 0;
-  auto is_fused = [&](const GPlan& g) {
-    return fuse && !g.small && g.m <= kFusedMaxM && g.n <= kFusedMaxN;
+  // -- matrices with 64 <= m <= 256 and n <= 512 run their NS rounds in one
+  //    kernel (after the grouped prologue, before the grouped apply) when no
+  //    matrix of the call needs the staged GEMM launches: the fused kernel and
+  //    the staged chain run one after the other, and beside a staged chain the
+  //    small matrices cost less as extra tiles of its stages
+  auto fusable = [](const GPlan& g) {
+    return !g.small && g.m <= kFusedMaxM && g.n <= kFusedMaxN;
   };
-  bool fused_launched = false;
-  {
-    FusedLaunch fl;
-    std::memset(&fl, 0, sizeof(fl));
-    fl.mode = sc.mode;
-    fl.steps = sc.steps;
-    fl.beta = sc.beta;
-    fl.a = sc.a;
-    fl.b = sc.b;
-    fl.c = sc.c;
-    fl.eps = sc.eps;
-    fl.decay = 1.0f - sc.lr * sc.wd;
-    fl.status = reinterpret_cast<unsigned int*>(ws);
-    double flops = 0, bytes = 0;
-    auto flush = [&]() -> muon_status {
-      if (fl.n_groups == 0) return MUON_OK;
-      const bool pdl = small_launched || fused_launched;
-      const cudaError_t e = tracked_launch(st, {MUON_K_FUSED_NS, -1, flops, bytes},
-                                           [&] { return launch_fused(fl, pdl, st); });
-      fl.n_groups = 0;
-      fl.total_clusters = 0;
-      flops = bytes = 0;
-      fused_launched = true;
-      return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
-    };
-    for (GPlan& g : gs) {
-      if (!is_fused(g) || g.batch == 0) continue;
-      FusedGroup& fg = fl.grp[fl.n_groups++];
-      fg.g = g.g;
-      fg.buf = g.buf;
-      fg.param = g.p;
-      fg.out = g.out;
-      fg.gdt = g.gdt;
-      fg.batch = g.batch;
-      fg.r = g.r;
-      fg.c = g.c;
-      fg.cluster_begin = fl.total_clusters;
-      const float scale = g.lr_scale > 0.f ? g.lr_scale
-                                            : static_cast<float>(std::sqrt(std::max(
-                                                  1.0, static_cast<double>(g.r) / g.c)));
-      fg.lr_eff = sc.lr * scale;
-      fl.total_clusters += g.batch;
-      const double mm = g.m, nn = g.n;
-      flops += static_cast<double>(g.batch) * sc.steps * (4.0 * mm * mm * nn + 2.0 * mm * mm * mm);
-      bytes += static_cast<double>(g.batch) * g.r * g.c *
-               ((g.gdt == MUON_BF16 ? 2.0 : 4.0) + (sc.mode == kPrologueNsOnly ? 2.0 : 16.0));
-      if (fl.n_groups == kMaxFusedGroups) {
-        s = flush();
-        if (s != MUON_OK) return s;
-      }
-    }
-    s = flush();
-    if (s != MUON_OK) return s;
-  }
+  bool fuse = g_fused_enabled.load(std::memory_order_relaxed) != 0;
+  for (const GPlan& g : gs)
+    if (g.batch > 0 && !g.small && !fusable(g)) fuse = false;
+  auto is_fused = [&](const GPlan& g) { return fuse && fusable(g); };
 
   // -- tensor-core matrices: one grouped prologue launch (per kMaxPrologueGroups)
   std::vector<GPlan*> big;
   for (GPlan& g : gs)
-    if (!g.small && !is_fused(g) && g.batch > 0) big.push_back(&g);
+    if (!g.small && g.batch > 0) big.push_back(&g);
   for (size_t c0 = 0; c0 < big.size(); c0 += kMaxPrologueGroups) {
     PrologueLaunch pl;
     std::memset(&pl, 0, sizeof(pl));
@@ -517,16 +468,66 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
                ((g.gdt == MUON_BF16 ? 2.0 : 4.0) + 2.0 + (sc.mode == kPrologueNsOnly ? 0.0 : 8.0));
     }
     pl.total_blocks = blocks;
-    const bool pdl = (small_launched || fused_launched) && c0 == 0;
+    const bool pdl = small_launched && c0 == 0;
     pl.wait_prior = pdl ? 1 : 0;
     const cudaError_t e = tracked_launch(st, {MUON_K_PROLOGUE, -1, 0.0, bytes},
                                          [&] { return launch_prologue(pl, sc.mode, pdl, st); });
     if (e != cudaSuccess) return MUON_ERR_CUDA;
   }
 
-  for (size_t c0 = 0; c0 < big.size(); c0 += kMaxProblems) {
-    std::vector<GPlan*> chunk(big.begin() + c0,
-                              big.begin() + std::min(big.size(), c0 + kMaxProblems));
+  // fused NS rounds: one CTA per matrix with m <= 128, a CTA pair for larger m
+  for (int pair = 0; pair < 2; ++pair) {
+    FusedLaunch fl;
+    std::memset(&fl, 0, sizeof(fl));
+    fl.pair = pair;
+    fl.steps = sc.steps;
+    fl.a = sc.a;
+    fl.b = sc.b;
+    fl.c = sc.c;
+    fl.eps = sc.eps;
+    fl.status = reinterpret_cast<unsigned int*>(ws);
+    double flops = 0;
+    auto flush = [&]() -> muon_status {
+      if (fl.n_groups == 0) return MUON_OK;
+      const cudaError_t e = tracked_launch(st, {MUON_K_FUSED_NS, -1, flops, 0.0},
+                                           [&] { return launch_fused(fl, st); });
+      fl.n_groups = 0;
+      fl.total_clusters = 0;
+      flops = 0;
+      return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+    };
+    for (GPlan* gp : big) {
+      const GPlan& g = *gp;
+      if (!is_fused(g) || (g.m > kTileM) != (pair == 1)) continue;
+      const int i = fl.n_groups++;
+      FusedGroup& fg = fl.grp[i];
+      fg.parts = reinterpret_cast<const float*>(ws + g.parts);
+      fg.nparts = g.nparts;
+      fg.batch = g.batch;
+      fg.m = g.m;
+      fg.n = g.n;
+      fg.cluster_begin = fl.total_clusters;
+      if (!operand_tmap(&fl.tm_x[i][0], ws + g.x0, g.n, g.m, g.batch, g.ldx, kTileM) ||
+          !operand_tmap(&fl.tm_x[i][1], ws + g.x1, g.n, g.m, g.batch, g.ldx, kTileM))
+        return MUON_ERR_CUDA;
+      fl.total_clusters += g.batch;
+      const double mm = g.m, nn = g.n;
+      flops += static_cast<double>(g.batch) * sc.steps * (4.0 * mm * mm * nn + 2.0 * mm * mm * mm);
+      if (fl.n_groups == kMaxFusedGroups) {
+        s = flush();
+        if (s != MUON_OK) return s;
+      }
+    }
+    s = flush();
+    if (s != MUON_OK) return s;
+  }
+
+  std::vector<GPlan*> staged;
+  for (GPlan* g : big)
+    if (!is_fused(*g)) staged.push_back(g);
+  for (size_t c0 = 0; c0 < staged.size(); c0 += kMaxProblems) {
+    std::vector<GPlan*> chunk(staged.begin() + c0,
+                              staged.begin() + std::min(staged.size(), c0 + kMaxProblems));
     for (int it = 0; it < sc.steps; ++it) {
       const int cur = it & 1;
       const bool first = (it == 0);

@@ -131,7 +131,8 @@ def test_ns5_fused_range_on_both_paths(shape, gdt, fused):
     n0 = muon.kernel_launch_count()
     with muon.fused_ns(fused):
         _check_ns5(shape, gdt)
-    assert (muon.kernel_launch_count() - n0 == 1) == fused
+    # fused: prologue, the fused rounds, apply; staged: prologue, 3 x 5 stages, apply
+    assert muon.kernel_launch_count() - n0 == (3 if fused else 17)
 
 
 def _check_ns5(shape, gdt):
@@ -319,8 +320,8 @@ def test_more_groups_than_one_launch_holds(fused):
     with muon.fused_ns(fused):
         muon.step_grouped(groups, momentum=0.95, lr=0.02, weight_decay=0.01)
     torch.cuda.synchronize()
-    if fused:
-        assert muon.kernel_launch_count() - n0 == 2
+    if fused:   # 17 groups: two launches each of prologue, fused rounds and apply
+        assert muon.kernel_launch_count() - n0 == 6
     for (P, G, B0), (pd, _, _) in zip(ref, groups):
         for i in range(P.shape[0]):
             p_ref, _, _ = oracle.muon_step(f64(P[i]), f64(G[i]), f64(B0[i]), momentum=0.95,
@@ -357,8 +358,9 @@ def test_launch_count_and_trace():
     muon.trace_begin(64)
     muon.ns5(G)
     recs = muon.trace_end()
-    assert muon.kernel_launch_count() - n0 == 1
-    assert [r["kind"] for r in recs] == ["fused_ns"] and recs[0]["ms"] > 0
+    assert muon.kernel_launch_count() - n0 == 3
+    assert [r["kind"] for r in recs] == ["prologue", "fused_ns", "apply"]
+    assert all(r["ms"] > 0 for r in recs)
     n0 = muon.kernel_launch_count()
     muon.trace_begin(64)
     with muon.fused_ns(False):
@@ -369,6 +371,27 @@ def test_launch_count_and_trace():
     assert kinds[0] == "prologue" and kinds[-1] == "apply"
     assert kinds[1:16] == ["gram", "poly", "update"] * 5
     assert all(r["ms"] > 0 for r in recs)
+
+
+def test_mixed_call_runs_every_matrix_staged():
+    # a call holding a matrix outside the fused range runs the fusable ones staged too
+    shapes = [(2, 128, 128), (1, 300, 520)]
+    groups, ref = [], []
+    for k, s in enumerate(shapes):
+        P, G = _rand(s, 0.02, torch.float32, 70 + k), _rand(s, 1e-3, torch.bfloat16, 80 + k)
+        ref.append((P, G))
+        groups.append((P.to(DEV), G.to(DEV), torch.zeros(s, device=DEV)))
+    n0 = muon.kernel_launch_count()
+    muon.trace_begin(64)
+    muon.step_grouped(groups, momentum=0.95, lr=0.02, weight_decay=0.01)
+    kinds = [r["kind"] for r in muon.trace_end()]
+    assert muon.kernel_launch_count() - n0 == 17 and "fused_ns" not in kinds
+    for (P, G), (pd, _, _) in zip(ref, groups):
+        for i in range(P.shape[0]):
+            p_ref, _, _ = oracle.muon_step(f64(P[i]), f64(G[i]), np.zeros(P.shape[1:]),
+                                           momentum=0.95, lr=0.02, weight_decay=0.01)
+            upd, upd_ref = f64(pd[i]) - 0.9998 * f64(P[i]), p_ref - 0.9998 * f64(P[i])
+            assert rel(upd, upd_ref) < NS_TOL
 
 
 def test_device_timeout_is_reported_and_the_context_stays_usable():
