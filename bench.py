@@ -431,6 +431,15 @@ def launches_per_step(step):
     return muon.kernel_launch_count() - n0
 
 
+# The sources each traced kernel is built from: a committed DRAM-traffic figure is
+# used only while these files are unchanged since it was captured.
+KERNEL_SOURCES = {
+    "gram": ("ns_gemm.cu", "ptx.cuh"), "poly": ("ns_gemm.cu", "ptx.cuh"),
+    "update": ("ns_gemm.cu", "ptx.cuh"), "prologue": ("prologue.cu",), "apply": ("prologue.cu",),
+    "small_ns": ("ns_small.cu",), "fused_ns": ("ns_fused.cu", "ptx.cuh"), "adam": ("adam.cu",),
+}
+
+
 def traffic_for(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it matches this build."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -438,18 +447,18 @@ def traffic_for(kernel: str, workload: str):
         with open(path) as f:
             d = json.load(f)
         e = d.get(f"{workload}/{kernel}")
-        if not e or e.get("source_hash") != source_hash():
+        if not e or e.get("source_hash") != source_hash(kernel):
             return None
         return e["dram_bytes_per_launch"]
     except (OSError, ValueError):
         return None
 
 
-def source_hash():
+def source_hash(kernel: str):
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "newton_schulz_step_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES.get(kernel, tuple(sorted(os.listdir(csrc)))):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
