@@ -115,8 +115,9 @@ struct GemmProblem {
 struct GemmLaunch {
   CUtensorMap tm_a[kMaxProblems];   // operand A tiles (box 64 x 128, 128-byte swizzle)
   CUtensorMap tm_b[kMaxProblems];   // operand B half tiles (box 64 x 128, or 64 x 64 for X)
+  CUtensorMap tm_at[kMaxProblems];  // symmetric operand A read transposed (box 64 x 64)
+  CUtensorMap tm_bt[kMaxProblems];  // Poly: symmetric operand B read transposed (box 64 x 64)
   CUtensorMap tm_out[kMaxProblems]; // output blocks (box 32 x 32 bf16, 64-byte swizzle)
-  CUtensorMap tm_mir[kMaxProblems]; // mirrored output blocks (box 32 x 32 bf16, no swizzle)
   CUtensorMap tm_in[kMaxProblems];  // Poly: blocks of A for the b A term (box 32 x 32, 64-byte swizzle)
   GemmProblem prob[kMaxProblems];
   int n_prob;

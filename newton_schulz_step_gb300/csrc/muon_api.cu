@@ -319,19 +319,22 @@ muon_status build_gemm(GemmLaunch& L, const std::vector<GPlan*>& chunk, int stag
     P.first_round = first_round ? 1 : 0;
     P.reverse = reverse ? 1 : 0;
     bool ok = true;
+    // (A and B' hold only the 256 x 256 tiles on or above the diagonal; the
+    // 64-row maps read the blocks below them at their transposed positions)
     if (stage == kStageGram) {          // A = s^2 X X^T
       ok = operand_tmap(&L.tm_a[i], xc, g.n, g.m, g.batch, g.ldx, kTileM) &&
            operand_tmap(&L.tm_b[i], xc, g.n, g.m, g.batch, g.ldx, kTileM) &&
-           output_tmap(&L.tm_out[i], ws + g.am, g.m, g.m, g.batch, g.lda, true) &&
-           output_tmap(&L.tm_mir[i], ws + g.am, g.m, g.m, g.batch, g.lda, false);
+           output_tmap(&L.tm_out[i], ws + g.am, g.m, g.m, g.batch, g.lda, true);
     } else if (stage == kStagePoly) {   // B' = a I + b A + c A A
       ok = operand_tmap(&L.tm_a[i], ws + g.am, g.m, g.m, g.batch, g.lda, kTileM) &&
            operand_tmap(&L.tm_b[i], ws + g.am, g.m, g.m, g.batch, g.lda, kTileM) &&
+           operand_tmap(&L.tm_at[i], ws + g.am, g.m, g.m, g.batch, g.lda, 64) &&
+           operand_tmap(&L.tm_bt[i], ws + g.am, g.m, g.m, g.batch, g.lda, 64) &&
            output_tmap(&L.tm_out[i], ws + g.bm, g.m, g.m, g.batch, g.lda, true) &&
-           output_tmap(&L.tm_mir[i], ws + g.bm, g.m, g.m, g.batch, g.lda, false) &&
            output_tmap(&L.tm_in[i], ws + g.am, g.m, g.m, g.batch, g.lda, true);
     } else {                            // X' = s B' X
       ok = operand_tmap(&L.tm_a[i], ws + g.bm, g.m, g.m, g.batch, g.lda, kTileM) &&
+           operand_tmap(&L.tm_at[i], ws + g.bm, g.m, g.m, g.batch, g.lda, 64) &&
            operand_tmap(&L.tm_b[i], xc, g.n, g.m, g.batch, g.ldx, 64) &&
            output_tmap(&L.tm_out[i], xn, g.n, g.m, g.batch, g.ldx, true);
     }

@@ -13,11 +13,15 @@
 // cost no accuracy against adding a X in fp32.
 //
 // X is m x n (m <= n) bf16, row-major with padded leading dimension; A and B
-// are m x m bf16.  A and B are symmetric, so Gram and Poly compute only the
-// tiles that hold entries on or above the diagonal and store every such entry
-// once directly and once mirrored.  For A A the second operand A[k][j] =
-// A[j][k] is then read K-major like the first; only the Update's X operand
-// (contraction over X's rows) is MN-major.
+// are m x m bf16.  A and B are symmetric, so Gram and Poly compute and store
+// only the 256 x 256 pair tiles on or above the diagonal (diagonal tiles
+// whole); nothing is ever written below them.  A consumer that needs a block
+// below (rows of pair row p, a K block in pair column q < p) loads the block
+// at the transposed position with TMA and hands it to the tensor cores as an
+// MN-major operand (the descriptor's major bit per k-block), so the stored
+// upper tiles serve both.  For A A the second operand A[k][j] = A[j][k] is read
+// the same way; the Update's X operand (contraction over X's rows) is always
+// MN-major.
 //
 // Kernel shape: persistent clusters of two CTAs (a CTA pair), one CTA per SM,
 // 192 threads:
@@ -25,7 +29,6 @@
 //   warp 1      TMEM allocator; in the even CTA also the tcgen05.mma issuer
 //   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator, fp32 math, 32 x 32
 //               blocks staged in shared memory and written by TMA bulk stores
-//               (Gram and Poly also store each block's mirror the same way)
 // The pair computes a 256 x 256 tile with cta_group::2 MMAs (M = 256): CTA r
 // holds tile rows 2p + r (128 rows of A) and the r-th 128-column half of B in
 // its own shared memory, and receives its 128 rows of the result in its own
@@ -43,12 +46,11 @@
 namespace muon {
 
 // Shared memory per CTA: the operand ring, the epilogue staging slots, barriers.
-// Poly reads its b A term through TMA into a third slot per warp, which it
-// pays for with one stage less in the ring (its MMA side waits least).
+// Poly reads its b A term through TMA into a third slot per warp.
 template <int STAGE>
 struct GemmCfg {
   static constexpr int kBN = 256;                        // pair tile: 256 x 256
-  static constexpr int kStages = STAGE == kStagePoly ? 5 : 6;
+  static constexpr int kStages = 6;
   static constexpr int kABytes = kTileM * kTileK * 2;    // 16 KB: 128 rows x 128 B
   static constexpr int kBBytes = (kBN / 2) * kTileK * 2; // 16 KB: this CTA's half of B
   static constexpr int kStageBytes = kABytes + kBBytes;  // 32 KB
@@ -56,7 +58,7 @@ struct GemmCfg {
   static constexpr int kEpiWarps = 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kSlots = STAGE == kStagePoly ? 3 : 2;  // per epilogue warp
-  static constexpr int kSlotBytes = 4096;
+  static constexpr int kSlotBytes = 2048;                // one 32 x 32 bf16 block
   static constexpr int kStagingBytes = kEpiWarps * kSlots * kSlotBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmem = kStages * kStageBytes + kStagingBytes + kBarBytes + 1024;
@@ -107,6 +109,19 @@ __device__ __forceinline__ void record_failure(const GemmLaunch& L, volatile int
   atomicOr(L.status, bit);
 }
 
+// Whether the k-block kb of an operand whose rows lie in pair row `pr` falls
+// below the stored upper tiles of a symmetric matrix (its pair column kb / 4 is
+// left of the diagonal), so it is read transposed.  Operand A is symmetric in
+// Poly (A) and Update (B'); operand B only in Poly.
+template <int STAGE>
+__device__ __forceinline__ bool a_transposed(int pr, int kb) {
+  return STAGE != kStageGram && pr > (kb * kTileK) / 256;
+}
+template <int STAGE>
+__device__ __forceinline__ bool b_transposed(int pr, int kb) {
+  return STAGE == kStagePoly && pr > (kb * kTileK) / 256;
+}
+
 __device__ __forceinline__ int first_tile() { return blockIdx.x >> 1; }
 __device__ __forceinline__ int tile_stride() { return gridDim.x >> 1; }
 
@@ -118,6 +133,8 @@ __device__ void run_producer(const GemmLaunch& L, uint8_t* smem, uint64_t* full,
   for (int p = 0; p < L.n_prob; ++p) {
     ptx::prefetch_tmap(&L.tm_a[p]);
     ptx::prefetch_tmap(&L.tm_b[p]);
+    if (STAGE != kStageGram) ptx::prefetch_tmap(&L.tm_at[p]);
+    if (STAGE == kStagePoly) ptx::prefetch_tmap(&L.tm_bt[p]);
   }
   int stage = 0;
   uint32_t phase = 0;
@@ -129,6 +146,8 @@ __device__ void run_producer(const GemmLaunch& L, uint8_t* smem, uint64_t* full,
     const GemmProblem& P = L.prob[tl.prob];
     const CUtensorMap* ta = &L.tm_a[tl.prob];
     const CUtensorMap* tb = &L.tm_b[tl.prob];
+    const CUtensorMap* tat = &L.tm_at[tl.prob];
+    const CUtensorMap* tbt = &L.tm_bt[tl.prob];
     for (int kb = 0; kb < P.k_blocks; ++kb) {
       // the pair's MMAs (issued by the even CTA) are done with this slot
       if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
@@ -141,8 +160,16 @@ __device__ void run_producer(const GemmLaunch& L, uint8_t* smem, uint64_t* full,
       // both CTAs' copies complete on the even CTA's barrier for this slot
       const uint32_t bar = leader_full0 + stage * 8;
       if (rank == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
-      // operand A: this CTA's 128 rows x 64 k-columns
-      ptx::tma_load_3d_pair(sa, ta, kb * kTileK, tl.tm * kTileM, tl.mat, bar);
+      // operand A: this CTA's 128 rows x 64 k-columns, or (below the stored
+      // tiles) the 64 x 128 block at the transposed position, MN-major
+      if (a_transposed<STAGE>(tl.tm >> 1, kb)) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          ptx::tma_load_3d_pair(sa + q * (64 * kTileK * 2), tat, tl.tm * kTileM + q * 64,
+                                kb * kTileK, tl.mat, bar);
+      } else {
+        ptx::tma_load_3d_pair(sa, ta, kb * kTileK, tl.tm * kTileM, tl.mat, bar);
+      }
       if (STAGE >= kStageUpdate) {
         // operand B = X[k][j], MN-major: this CTA's 128 columns as 2 slabs of
         // 64 columns x 64 k-rows
@@ -150,6 +177,12 @@ __device__ void run_producer(const GemmLaunch& L, uint8_t* smem, uint64_t* full,
         for (int q = 0; q < 2; ++q)
           ptx::tma_load_3d_pair(sb + q * (64 * kTileK * 2), tb, tl.tn * C::kBN + rank * 128 + q * 64,
                                 kb * kTileK, tl.mat, bar);
+      } else if (b_transposed<STAGE>(tl.tn, kb)) {
+        // Poly, below the stored tiles: the transposed block, MN-major
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          ptx::tma_load_3d_pair(sb + q * (64 * kTileK * 2), tbt,
+                                tl.tn * C::kBN + rank * kTileM + q * 64, kb * kTileK, tl.mat, bar);
       } else {
         // operand B: this CTA's 128 of the tile column's 256 rows, K-major
         ptx::tma_load_3d_pair(sb, tb, kb * kTileK, tl.tn * C::kBN + rank * kTileM, tl.mat, bar);
@@ -178,7 +211,6 @@ __device__ void run_mma(const GemmLaunch& L, uint8_t* smem, uint64_t* full, uint
                         uint32_t tmem_base, volatile int* abort_flag) {
   using C = GemmCfg<STAGE>;
   constexpr bool kBmn = (STAGE >= kStageUpdate);
-  constexpr uint32_t kIdesc = ptx::idesc_bf16(2 * kTileM, C::kBN, kBmn);
   int stage = 0;
   uint32_t phase = 0;
   int acc = 0;
@@ -204,15 +236,19 @@ __device__ void run_mma(const GemmLaunch& L, uint8_t* smem, uint64_t* full, uint
       }
       const uint32_t sa = ptx::smem_u32(smem + stage * C::kStageBytes);
       const uint32_t sb = sa + C::kABytes;
+      const bool a_mn = a_transposed<STAGE>(tl.tm >> 1, kb);
+      const bool b_mn = kBmn || b_transposed<STAGE>(tl.tn, kb);
+      const uint32_t idesc = ptx::idesc_bf16(2 * kTileM, C::kBN, b_mn, a_mn);
 #pragma unroll
       for (int k = 0; k < kTileK / 16; ++k) {
         // K-major SW128: 8-row groups 1024 B apart; a K=16 slice is 32 B on.
-        const uint64_t da = ptx::smem_desc_sw128(sa + k * 32, 16, 1024);
-        // MN-major SW128: 64-column slabs (64 x 128 B) apart along N, 8-row
-        // groups 1024 B apart along K; a K=16 slice is 16 rows = 2048 B on.
-        const uint64_t db = kBmn ? ptx::smem_desc_sw128(sb + k * 2048, 64 * kTileK * 2, 1024)
+        // MN-major SW128: 64-column slabs (64 x 128 B) apart along M or N,
+        // 8-row groups 1024 B apart along K; a K=16 slice is 16 rows = 2048 B on.
+        const uint64_t da = a_mn ? ptx::smem_desc_sw128(sa + k * 2048, 64 * kTileK * 2, 1024)
+                                 : ptx::smem_desc_sw128(sa + k * 32, 16, 1024);
+        const uint64_t db = b_mn ? ptx::smem_desc_sw128(sb + k * 2048, 64 * kTileK * 2, 1024)
                                  : ptx::smem_desc_sw128(sb + k * 32, 16, 1024);
-        ptx::mma_bf16_pair(d_tmem, da, db, kIdesc, (kb | k) != 0 ? 1u : 0u);
+        ptx::mma_bf16_pair(d_tmem, da, db, idesc, (kb | k) != 0 ? 1u : 0u);
       }
       // frees the slot in both CTAs once these MMAs have read it
       ptx::mma_commit_pair(&empty[stage]);
@@ -301,8 +337,7 @@ __device__ __forceinline__ void stage_row_sw64(uint8_t* blk, int r, const float 
 
 // ------------------------------------------------------------ epilogue warps
 // Warp w (2..5) owns TMEM lanes 32*(w&3).. (32 rows of the 128-row tile) and
-// walks the tile's 256 columns in 8 chunks of 32.  Symmetric stages skip the
-// chunks wholly below the diagonal (their entries come from mirrors).
+// walks the tile's 256 columns in 8 chunks of 32.
 template <int STAGE>
 __device__ void run_epilogue(const GemmLaunch& L, uint64_t* acc_full, uint64_t* acc_empty,
                              uint64_t* in_bar, uint32_t tmem_base, uint8_t* staging,
@@ -323,7 +358,6 @@ __device__ void run_epilogue(const GemmLaunch& L, uint64_t* acc_full, uint64_t* 
     const Tile tl = decode_tile<STAGE>(L, t, rank);
     const GemmProblem& P = L.prob[tl.prob];
     const CUtensorMap* tm_out = &L.tm_out[tl.prob];
-    const CUtensorMap* tm_mir = &L.tm_mir[tl.prob];
     const CUtensorMap* tm_in = &L.tm_in[tl.prob];
     float s = 1.f;
     if (STAGE != kStagePoly && P.first_round)
@@ -331,13 +365,9 @@ __device__ void run_epilogue(const GemmLaunch& L, uint64_t* acc_full, uint64_t* 
     const int i0 = tl.tm * kTileM + quarter * 32;  // first row of this warp
     const int ncols = kSym ? P.m : P.n;
     const int jt = tl.tn * C::kBN;
-    // live chunks: c_lo <= ch < c_hi (rows in range, columns in range, and for
-    // symmetric stages not wholly below the diagonal)
-    int c_lo = 0, c_hi = 0;
-    if (i0 < P.m) {
-      c_hi = min(kChunks, (ncols - jt + 31) / 32);
-      if (kSym) c_lo = max(0, (i0 - jt) / 32);
-    }
+    // live chunks: c_lo <= ch < c_hi (rows in range, columns in range)
+    const int c_lo = 0;
+    const int c_hi = i0 < P.m ? min(kChunks, (ncols - jt + 31) / 32) : 0;
     // Poly: the first two live chunks' A blocks into their slots
     if constexpr (kPoly) {
       if (lane == 0) {
@@ -366,7 +396,6 @@ __device__ void run_epilogue(const GemmLaunch& L, uint64_t* acc_full, uint64_t* 
     for (int ch = c_lo; ch < c_hi; ++ch) {
       const int j0 = jt + ch * 32;
       uint8_t* blk = my_slots + slot * C::kSlotBytes;
-      uint8_t* mir = blk + 2048;
       uint32_t ev[16];
       if constexpr (kPoly) {
         const uint32_t par = (in_par >> slot) & 1u;
@@ -410,30 +439,11 @@ __device__ void run_epilogue(const GemmLaunch& L, uint64_t* acc_full, uint64_t* 
         for (int q = 0; q < 32; ++q) val[q] = s * __uint_as_float(v[q]);
       }
 
-      const bool diag = kSym && j0 == i0;
-      if (!diag) {
-        stage_row_sw64(blk, lane, val);
-        if constexpr (kSym) {
-#pragma unroll
-          for (int q = 0; q < 32; ++q)
-            *reinterpret_cast<__nv_bfloat16*>(mir + q * 64 + lane * 2) =
-                __float2bfloat16_rn(val[q]);
-        }
-      } else {
-        // diagonal block: assemble it whole; entry (r, c) with c >= r comes
-        // from thread r, its mirror (c, r) from the same value
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const __nv_bfloat16 h = __float2bfloat16_rn(val[q]);
-          if (q >= lane) *reinterpret_cast<__nv_bfloat16*>(blk + sw64(lane, q)) = h;
-          if (q > lane) *reinterpret_cast<__nv_bfloat16*>(blk + sw64(q, lane)) = h;
-        }
-      }
+      stage_row_sw64(blk, lane, val);
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         ptx::tma_store_3d(tm_out, j0, i0, tl.mat, blk);
-        if (kSym && !diag) ptx::tma_store_3d(tm_mir, i0, j0, tl.mat, mir);
         ptx::bulk_commit();
         // Poly: the A block two live chunks ahead goes into the slot whose
         // store was issued one chunk ago

@@ -395,9 +395,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 // Instruction descriptor for kind::f16 with bf16 A/B, fp32 D.
 // Bits: D format 4-5 (1 = f32), A format 7-9 (1 = bf16), B format 10-12,
 // A major 15, B major 16 (1 = MN-major), N >> 3 in 17-22, M >> 4 in 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-         ((static_cast<uint32_t>(n) >> 3) << 17) | ((static_cast<uint32_t>(m) >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn_major,
+                                                  bool a_mn_major = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | ((static_cast<uint32_t>(n) >> 3) << 17) |
+         ((static_cast<uint32_t>(m) >> 4) << 24);
 }
 
 }  // namespace ptx

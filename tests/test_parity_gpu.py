@@ -63,7 +63,8 @@ def test_prologue_writes_u_then_gram_and_poly(shape, gdt):
     """steps=1 leaves X0 = bf16(u or u^T), A = s^2 X0 X0^T and B' = aI + bA + cA^2 in the workspace.
 
     (The polynomial stage folds the a X term of the update into its output, so
-    the update is the single product B' X.)"""
+    the update is the single product B' X.  A and B' are symmetric and only their
+    256 x 256 tiles on or above the diagonal are stored; those are compared.)"""
     b, r, c = shape
     m, n = min(r, c), max(r, c)
     ldx, lda = (n + 7) // 8 * 8, (m + 7) // 8 * 8
@@ -93,10 +94,13 @@ def test_prologue_writes_u_then_gram_and_poly(shape, gdt):
         x = f64(X0[i])
         s = 1.0 / (np.linalg.norm(u) + 1e-7)
         A_ref = s * s * (x @ x.T)
-        assert rel(f64(A[i]), A_ref) < 8e-3
-        a_ = f64(A[i])
+        tiles = np.arange(m) // 256
+        stored = tiles[:, None] <= tiles[None, :]
+        assert rel(f64(A[i])[stored], A_ref[stored]) < 8e-3
+        a_up = np.where(stored, f64(A[i]), 0.0)
+        a_ = np.triu(a_up) + np.triu(a_up, 1).T          # the symmetric A the stored tiles define
         B_ref = muon.COEFFS[0] * np.eye(m) + muon.COEFFS[1] * a_ + muon.COEFFS[2] * (a_ @ a_)
-        assert rel(f64(Bm[i]), B_ref) < 2e-2
+        assert rel(f64(Bm[i])[stored], B_ref[stored]) < 2e-2
 
 
 # ------------------------------------------------------------ NS only
