@@ -292,7 +292,7 @@ def run_gpu(args, wl):
         k["n"] += 1
         k["flops"] += r["flops"]
         k["bytes"] += r["bytes"]
-    ns_kinds = ("gram", "poly", "update", "small_ns", "fused_ns")
+    ns_kinds = ("gram", "poly", "update", "small_ns", "fused_ns", "rounds")
     ns_ms = sum(kinds[k]["ms"] for k in ns_kinds if k in kinds) / args.steps
     traced_ms = sum(k["ms"] for k in kinds.values()) / args.steps
     dom_name, dom = max(kinds.items(), key=lambda kv: kv[1]["ms"])

@@ -79,8 +79,10 @@ typedef enum muon_kernel_kind {
   MUON_K_UPDATE = 4,     /* X <- s B' X  (= s (a X + B X))                      */
   MUON_K_APPLY = 5,      /* p <- (1 - lr wd) p - lr scale O (or O as bf16)      */
   MUON_K_ADAM = 6,       /* DistAdam update of non-matrix parameters            */
-  MUON_K_FUSED_NS = 7    /* all NS rounds, one CTA pair per matrix, 64<=m<=256,
+  MUON_K_FUSED_NS = 7,   /* all NS rounds, one CTA pair per matrix, 64<=m<=256,
                             n<=512 (see muon_set_fused_ns)                      */
+  MUON_K_ROUNDS = 8      /* all Gram/Poly/Update stages of every round in one
+                            persistent launch (see muon_set_persistent_rounds)  */
 } muon_kernel_kind;
 
 /* Workspace bytes for one muon_step()/muon_ns5() call on [batch, rows, cols].
@@ -219,6 +221,22 @@ muon_status muon_adam_step(const muon_adam_tensor* tensors, int n_tensors, int s
  * changed) if enable is not 0 or 1.
  */
 int muon_set_fused_ns(int enable);
+
+/*
+ * Launch structure of the tensor-core NS rounds (no counterpart on the pages).
+ * mode = 0: one grouped launch per stage and round (Gram, Poly, Update; 15
+ * launches for five rounds), each waiting for the one before.
+ * mode = 1: one persistent launch covers every stage of every round; a tile
+ * starts as soon as the tiles of the stages before it of the same matrix are
+ * stored (per-matrix completion counters in the workspace), so one matrix's
+ * next stage overlaps other matrices' current one.
+ * mode = 2 (the default): 1 for groups whose rounds are short (estimated
+ * tensor-core time of a round under 400 us), where the stage boundaries weigh
+ * most; 0 otherwise.  Same results and workspace size in every mode.
+ * Process-wide; affects calls made afterwards.  Returns the previous mode, or
+ * -1 (nothing changed) if mode is not 0, 1 or 2.
+ */
+int muon_set_persistent_rounds(int mode);
 
 /* Static English text for a status code. */
 const char* muon_status_string(muon_status status);

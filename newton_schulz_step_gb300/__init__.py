@@ -25,7 +25,7 @@ __all__ = [
     "grouped_workspace_bytes", "Workspace", "ns5", "step", "step_noalloc", "step_grouped",
     "GroupedStep", "AdamStep", "adam_step", "ADAM_LR", "ADAM_BETAS", "ADAM_EPS",
     "workspace_status", "status_string", "kernel_launch_count", "trace_begin", "trace_end",
-    "set_fused_ns", "fused_ns",
+    "set_fused_ns", "fused_ns", "set_persistent_rounds", "persistent_rounds",
     "KERNEL_KINDS",
 ]
 
@@ -40,7 +40,7 @@ ADAM_BETAS = (0.8, 0.95)
 ADAM_EPS = 1e-8
 
 KERNEL_KINDS = {0: "prologue", 1: "small_ns", 2: "gram", 3: "poly", 4: "update", 5: "apply",
-                6: "adam", 7: "fused_ns"}
+                6: "adam", 7: "fused_ns", 8: "rounds"}
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "timeout",
            5: "workspace"}
 
@@ -108,6 +108,8 @@ def load_library():
     L.muon_selftest_wait_timeout.restype = ci
     L.muon_adam_step.argtypes = [ctypes.POINTER(_AdamTensor), ci, ci, cf, cf, cf, cf, cf, vp]
     L.muon_adam_step.restype = ci
+    L.muon_set_persistent_rounds.argtypes = [ci]
+    L.muon_set_persistent_rounds.restype = ci
     L.muon_set_fused_ns.argtypes = [ci]
     L.muon_set_fused_ns.restype = ci
     L.muon_status_string.argtypes = [ci]
@@ -398,6 +400,34 @@ def set_fused_ns(enable: bool) -> bool:
     if prev < 0:
         raise MuonError(1, "muon_set_fused_ns")
     return bool(prev)
+
+
+def set_persistent_rounds(mode) -> int:
+    """Launch structure of the tensor-core NS rounds: True/1 one persistent launch,
+    False/0 one launch per stage and round, "auto"/2 (the default) persistent when
+    a round is short; returns the previous mode (0, 1 or 2)."""
+    m = 2 if mode == "auto" else int(mode)
+    prev = int(load_library().muon_set_persistent_rounds(m))
+    if prev < 0:
+        raise MuonError(1, "muon_set_persistent_rounds")
+    return prev
+
+
+class persistent_rounds:
+    """Context manager: `with persistent_rounds(True): ...` runs the block with the
+    persistent rounds kernel."""
+
+    def __init__(self, mode):
+        self.mode = mode
+        self.prev = None
+
+    def __enter__(self):
+        self.prev = set_persistent_rounds(self.mode)
+        return self
+
+    def __exit__(self, *exc):
+        set_persistent_rounds(self.prev)
+        return False
 
 
 class fused_ns:

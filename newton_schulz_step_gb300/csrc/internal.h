@@ -27,6 +27,7 @@ enum DeviceError : unsigned int {
   kErrTimeoutEpilogue = 4u,
   kErrTimeoutDrain = 8u,
   kErrTimeoutFused = 16u,
+  kErrTimeoutDepend = 32u,
 };
 
 // What the prologue computes from (g, buf).
@@ -54,6 +55,8 @@ struct PrologueLaunch {
   int total_blocks;
   float beta;
   int wait_prior;         // 1: wait for the preceding grid (PDL) before exiting
+  unsigned int* zero;     // counters the launch zeroes (block 0), or null
+  int n_zero;
 };
 
 // One tensor-core group of the grouped apply launch: the NS result O (bf16,
@@ -128,6 +131,44 @@ struct GemmLaunch {
 
 enum GemmStage : int { kStageGram = 0, kStagePoly = 1, kStageUpdate = 2 };
 
+// ---- all NS rounds of a chunk of groups in one persistent launch (ns_gemm.cu)
+// Work items are the pair tiles of every (round, stage), in round-major, then
+// stage, then problem, matrix and tile order; a tile of stage s of round r of a
+// matrix starts once every tile of the stages before it (of that matrix) is
+// stored, which per-matrix completion counters in the workspace track.
+struct RoundsProblem {
+  int batch, m, n;
+  int tiles_m;            // pair rows: ceil(ceil(m / 128) / 2)
+  int tiles_n[3];         // 256-wide tile columns of each stage's output
+  int tiles_per_mat[3];   // pair tiles per matrix in each stage
+  int tile_begin[3];      // first tile of this problem within each stage
+  int k_blocks[3];        // ceil(K / kTileK) per stage
+  const float* parts;     // norm partials [batch, nparts]
+  int nparts;
+  int done_begin;         // this problem's first matrix counter
+};
+
+struct RoundsLaunch {
+  CUtensorMap x_op[kMaxProblems][2];   // X buffer 0/1 as K-major operand (box 64 x 128)
+  CUtensorMap x_mn[kMaxProblems][2];   // X buffer 0/1 as MN-major operand (box 64 x 64)
+  CUtensorMap x_out[kMaxProblems][2];  // X buffer 0/1 output blocks (32 x 32, 64-byte swizzle)
+  CUtensorMap a_op[kMaxProblems];      // A (box 64 x 128)
+  CUtensorMap a_mn[kMaxProblems];      // A read transposed (box 64 x 64)
+  CUtensorMap a_blk[kMaxProblems];     // A 32 x 32 blocks (Gram output, Poly b A input)
+  CUtensorMap b_op[kMaxProblems];      // B' (box 64 x 128)
+  CUtensorMap b_mn[kMaxProblems];      // B' read transposed (box 64 x 64)
+  CUtensorMap b_out[kMaxProblems];     // B' 32 x 32 output blocks
+  RoundsProblem prob[kMaxProblems];
+  int n_prob;
+  int steps;
+  int stage_tiles[3];     // pair tiles of one stage over all problems
+  int round_tiles;        // sum of stage_tiles
+  int total_items;        // steps * round_tiles
+  unsigned int* done;     // per-matrix completion counters, zeroed by the prologue
+  float a, b, c, eps;
+  unsigned int* status;   // sticky device error word
+};
+
 // ---- fused NS kernel for 64 <= m <= 256, n <= 512 (ns_fused.cu): all rounds
 // of one matrix on one CTA pair; X0 and the norm partials come from the
 // grouped prologue, the result O goes where the staged path leaves it
@@ -189,6 +230,8 @@ cudaError_t launch_apply(const ApplyLaunch& l, bool to_param, cudaStream_t s);
 // One launch of a GEMM stage over `pair_tiles` cluster tiles (two 128 x 256
 // CTA tiles each); the grid is sized from the device's SM count.
 cudaError_t launch_gemm(const GemmLaunch& l, int stage, int pair_tiles, int sms, cudaStream_t s);
+// All rounds of the problems of `l` in one launch (grid sized from the SM count).
+cudaError_t launch_rounds(const RoundsLaunch& l, int sms, cudaStream_t s);
 int gemm_smem_bytes();
 cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_ns,
                                  cudaStream_t s);

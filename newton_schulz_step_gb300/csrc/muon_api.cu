@@ -29,6 +29,16 @@ namespace {
 std::atomic<unsigned long long> g_launch_count{0};
 // 1: matrices with 64 <= m <= 256 and n <= 512 take the one-kernel fused path
 std::atomic<int> g_fused_enabled{1};
+// NS rounds of tensor-core groups: 0 one launch per stage and round, 1 one
+// persistent launch per chunk, 2 (default) persistent when a round is short
+std::atomic<int> g_rounds_enabled{2};
+
+// The persistent launch pays off while stage boundaries (launch, pipeline fill,
+// last-wave tail: a few microseconds each) weigh on a round; on rounds of
+// milliseconds it was measured slower (d=2048 model: 37.4 vs 31.3 ms per
+// step).  Estimated tensor-core time of one round of a chunk, in microseconds:
+// 512 clocks per pair tile and 64-deep k-block, at ~1.9 GHz on sms / 2 pairs
+// (round_mma_us below).
 
 struct TraceSlot {
   cudaEvent_t e0 = nullptr, e1 = nullptr;
@@ -166,6 +176,7 @@ struct GPlan {
   bool tall = false, small = false;
   int ldx = 0, lda = 0, nparts = 0;
   size_t x0 = 0, x1 = 0, am = 0, bm = 0, parts = 0, xs = 0;  // workspace offsets
+  int ctr = 0;  // first per-matrix completion counter (persistent rounds kernel)
 };
 
 constexpr size_t kStatusBytes = 256;
@@ -180,8 +191,18 @@ bool shape_ok(int batch, int r, int c) {
 }
 
 // Fills the derived fields and workspace offsets; returns the total bytes.
+// Layout: the status block, the per-matrix completion counters of every
+// tensor-core matrix (one u32 each), then each group's buffers.
 size_t plan_workspace(std::vector<GPlan>& gs) {
-  size_t off = kStatusBytes;
+  int counters = 0;
+  for (GPlan& g : gs) {
+    g.m = std::min(g.r, g.c);
+    if (g.batch > 0 && g.m > kSmallMaxM) {
+      g.ctr = counters;
+      counters += g.batch;
+    }
+  }
+  size_t off = kStatusBytes + (counters ? align256(static_cast<size_t>(counters) * 4) : 0);
   for (GPlan& g : gs) {
     g.tall = g.r > g.c;
     g.m = std::min(g.r, g.c);
@@ -350,6 +371,76 @@ muon_status build_gemm(GemmLaunch& L, const std::vector<GPlan*>& chunk, int stag
   return MUON_OK;
 }
 
+constexpr double kPersistentRoundUs = 400.0;
+
+double round_mma_us(const std::vector<GPlan*>& chunk, int sms) {
+  double kblocks = 0;
+  for (const GPlan* g : chunk)
+    for (int stage = 0; stage < 3; ++stage) {
+      const StageShape ss = stage_shape(*g, stage);
+      kblocks += static_cast<double>(g->batch) * ss.tiles_per_mat * ss.k_blocks;
+    }
+  const double pairs = std::max(1, sms / 2);
+  return kblocks * 512.0 / pairs / 1.9e3;
+}
+
+// Builds the launch block of the persistent rounds kernel for a chunk of
+// tensor-core groups: every stage walks the groups by ascending n and each
+// group's matrices in order, so a matrix's next stage follows its current one.
+muon_status build_rounds(RoundsLaunch& R, const std::vector<GPlan*>& chunk, const Scalars& sc,
+                         uint8_t* ws) {
+  std::memset(&R, 0, sizeof(R));
+  std::vector<GPlan*> order(chunk);
+  std::stable_sort(order.begin(), order.end(),
+                   [](GPlan* x, GPlan* y) { return x->n < y->n; });
+  int begin[3] = {0, 0, 0};
+  for (size_t i = 0; i < order.size(); ++i) {
+    const GPlan& g = *order[i];
+    RoundsProblem& P = R.prob[i];
+    P.batch = g.batch;
+    P.m = g.m;
+    P.n = g.n;
+    for (int stage = 0; stage < 3; ++stage) {
+      const StageShape ss = stage_shape(g, stage);
+      P.tiles_m = ss.tiles_m;
+      P.tiles_n[stage] = ss.tiles_n;
+      P.tiles_per_mat[stage] = ss.tiles_per_mat;
+      P.k_blocks[stage] = ss.k_blocks;
+      P.tile_begin[stage] = begin[stage];
+      begin[stage] += ss.tiles_per_mat * g.batch;
+    }
+    P.parts = reinterpret_cast<const float*>(ws + g.parts);
+    P.nparts = g.nparts;
+    P.done_begin = g.ctr;
+    bool ok = true;
+    for (int b = 0; b < 2; ++b) {
+      uint8_t* xb = ws + (b ? g.x1 : g.x0);
+      ok = ok && operand_tmap(&R.x_op[i][b], xb, g.n, g.m, g.batch, g.ldx, kTileM) &&
+           operand_tmap(&R.x_mn[i][b], xb, g.n, g.m, g.batch, g.ldx, 64) &&
+           output_tmap(&R.x_out[i][b], xb, g.n, g.m, g.batch, g.ldx, true);
+    }
+    ok = ok && operand_tmap(&R.a_op[i], ws + g.am, g.m, g.m, g.batch, g.lda, kTileM) &&
+         operand_tmap(&R.a_mn[i], ws + g.am, g.m, g.m, g.batch, g.lda, 64) &&
+         output_tmap(&R.a_blk[i], ws + g.am, g.m, g.m, g.batch, g.lda, true) &&
+         operand_tmap(&R.b_op[i], ws + g.bm, g.m, g.m, g.batch, g.lda, kTileM) &&
+         operand_tmap(&R.b_mn[i], ws + g.bm, g.m, g.m, g.batch, g.lda, 64) &&
+         output_tmap(&R.b_out[i], ws + g.bm, g.m, g.m, g.batch, g.lda, true);
+    if (!ok) return MUON_ERR_CUDA;
+  }
+  R.n_prob = static_cast<int>(order.size());
+  R.steps = sc.steps;
+  for (int stage = 0; stage < 3; ++stage) R.stage_tiles[stage] = begin[stage];
+  R.round_tiles = begin[0] + begin[1] + begin[2];
+  R.total_items = sc.steps * R.round_tiles;
+  R.done = reinterpret_cast<unsigned int*>(ws + kStatusBytes);
+  R.a = sc.a;
+  R.b = sc.b;
+  R.c = sc.c;
+  R.eps = sc.eps;
+  R.status = reinterpret_cast<unsigned int*>(ws);
+  return MUON_OK;
+}
+
 // ------------------------------------------------------------ the step
 muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
                      size_t ws_bytes, cudaStream_t st) {
@@ -473,6 +564,12 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
     pl.total_blocks = blocks;
     const bool pdl = small_launched && c0 == 0;
     pl.wait_prior = pdl ? 1 : 0;
+    if (c0 == 0) {  // the persistent rounds kernel's completion counters start at zero
+      pl.zero = reinterpret_cast<unsigned int*>(ws + kStatusBytes);
+      int n = 0;
+      for (const GPlan* g : big) n += g->batch;
+      pl.n_zero = n;
+    }
     const cudaError_t e = tracked_launch(st, {MUON_K_PROLOGUE, -1, 0.0, bytes},
                                          [&] { return launch_prologue(pl, sc.mode, pdl, st); });
     if (e != cudaSuccess) return MUON_ERR_CUDA;
@@ -528,9 +625,26 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
   std::vector<GPlan*> staged;
   for (GPlan* g : big)
     if (!is_fused(*g)) staged.push_back(g);
+  const int rounds_mode = g_rounds_enabled.load(std::memory_order_relaxed);
   for (size_t c0 = 0; c0 < staged.size(); c0 += kMaxProblems) {
     std::vector<GPlan*> chunk(staged.begin() + c0,
                               staged.begin() + std::min(staged.size(), c0 + kMaxProblems));
+    const bool persistent =
+        rounds_mode == 1 || (rounds_mode == 2 && round_mma_us(chunk, sms) < kPersistentRoundUs);
+    if (persistent) {
+      RoundsLaunch R;
+      s = build_rounds(R, chunk, sc, ws);
+      if (s != MUON_OK) return s;
+      if (R.total_items == 0) continue;
+      double flops = 0;
+      for (GPlan* g : chunk)
+        for (int stage = 0; stage < 3; ++stage) flops += stage_flops(*g, stage);
+      flops *= sc.steps;
+      const cudaError_t e = tracked_launch(st, {MUON_K_ROUNDS, -1, flops, 0.0},
+                                           [&] { return launch_rounds(R, sms, st); });
+      if (e != cudaSuccess) return MUON_ERR_CUDA;
+      continue;
+    }
     for (int it = 0; it < sc.steps; ++it) {
       const int cur = it & 1;
       const bool first = (it == 0);
@@ -807,6 +921,11 @@ const char* muon_status_string(muon_status status) {
       return "workspace missing, misaligned or too small";
   }
   return "unknown status";
+}
+
+int muon_set_persistent_rounds(int enable) {
+  if (enable < 0 || enable > 2) return -1;
+  return g_rounds_enabled.exchange(enable);
 }
 
 int muon_set_fused_ns(int enable) {

@@ -40,15 +40,25 @@
 // upper-triangle tiles, so symmetric stages pair up exactly.  The accumulator
 // is double buffered in TMEM so the epilogue of one tile overlaps the MMAs of
 // the next.
+//
+// Two kernels share these roles, tile by tile:
+//   ns_gemm_kernel<stage>  one stage of one round over a chunk of groups (one
+//                          launch per stage, chained by programmatic
+//                          dependent launch)
+//   ns_rounds_kernel       every stage of every round of a chunk of groups in
+//                          one launch: a tile waits (in the producer) for the
+//                          per-matrix completion counter of the stages before
+//                          it, which the epilogue warps advance once their
+//                          stores of a tile are complete, so one matrix's
+//                          next stage can start while other matrices still
+//                          finish the current one.
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace muon {
 
 // Shared memory per CTA: the operand ring, the epilogue staging slots, barriers.
-// Poly reads its b A term through TMA into a third slot per warp.
-template <int STAGE>
-struct GemmCfg {
+struct Cfg {
   static constexpr int kBN = 256;                        // pair tile: 256 x 256
   static constexpr int kStages = 6;
   static constexpr int kABytes = kTileM * kTileK * 2;    // 16 KB: 128 rows x 128 B
@@ -57,57 +67,33 @@ struct GemmCfg {
   static constexpr int kTmemCols = 2 * kBN;              // two 128 x 256 fp32 accumulators
   static constexpr int kEpiWarps = 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
-  static constexpr int kSlots = STAGE == kStagePoly ? 3 : 2;  // per epilogue warp
+  static constexpr int kSlots = 3;                       // per epilogue warp
   static constexpr int kSlotBytes = 2048;                // one 32 x 32 bf16 block
   static constexpr int kStagingBytes = kEpiWarps * kSlots * kSlotBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmem = kStages * kStageBytes + kStagingBytes + kBarBytes + 1024;
+  // completion-counter increments per stored pair tile: every epilogue warp of both CTAs
+  static constexpr unsigned int kSignalsPerTile = 2 * kEpiWarps;
 };
 
-struct Tile {
-  int prob, mat, tm, tn;  // tm: this CTA's tile row (2 * pair row + cluster rank)
+// Everything a role needs to know about one pair tile.
+struct TileCtx {
+  const CUtensorMap* a;    // operand A, K-major boxes of 64 x 128
+  const CUtensorMap* at;   // operand A read transposed (symmetric A), boxes of 64 x 64
+  const CUtensorMap* b;    // operand B: K-major 64 x 128 (Gram, Poly) or 64 x 64 (Update, X)
+  const CUtensorMap* bt;   // Poly: operand B read transposed, 64 x 64
+  const CUtensorMap* out;  // output 32 x 32 blocks
+  const CUtensorMap* in;   // Poly: A 32 x 32 blocks (the b A term)
+  int mat, pr, tn;         // matrix, pair row (pr >= tiles_m: no rows), tile column
+  int m, n, k_blocks;
+  const float* parts;      // first round: norm partials of the batch
+  int nparts;
+  int first_round;
 };
 
-// Linear pair-tile index -> (problem, matrix, tile row of this CTA, tile col).
-// Symmetric stages enumerate, per pair row p, the tile columns tn >= p.
-template <int STAGE>
-__device__ __forceinline__ Tile decode_tile(const GemmLaunch& L, int t, int rank) {
-  int p = 0;
-#pragma unroll 1
-  while (p + 1 < L.n_prob && t >= L.prob[p + 1].tile_begin) ++p;
-  const GemmProblem& P = L.prob[p];
-  const int local = t - P.tile_begin;
-  Tile r;
-  r.prob = p;
-  r.mat = local / P.tiles_per_mat;
-  int w = local - r.mat * P.tiles_per_mat;
-  if (P.reverse) r.mat = P.batch - 1 - r.mat;
-  int tp = P.tiles_m;  // out of range unless found (no stores then)
-  if (STAGE >= kStageUpdate) {
-    tp = w / P.tiles_n;
-    r.tn = w - tp * P.tiles_n;
-  } else {
-    r.tn = 0;
-#pragma unroll 1
-    for (int q = 0; q < P.tiles_m; ++q) {
-      const int cnt = P.tiles_n - q;
-      if (w < cnt) {
-        tp = q;
-        r.tn = q + w;
-        break;
-      }
-      w -= cnt;
-    }
-  }
-  r.tm = 2 * tp + rank;
-  return r;
-}
-
-__device__ __forceinline__ void record_failure(const GemmLaunch& L, volatile int* abort_flag,
-                                               unsigned int bit) {
-  *abort_flag = 1;
-  atomicOr(L.status, bit);
-}
+struct GemmScalars {
+  float a, b, c, eps;
+};
 
 // Whether the k-block kb of an operand whose rows lie in pair row `pr` falls
 // below the stored upper tiles of a symmetric matrix (its pair column kb / 4 is
@@ -122,151 +108,142 @@ __device__ __forceinline__ bool b_transposed(int pr, int kb) {
   return STAGE == kStagePoly && pr > (kb * kTileK) / 256;
 }
 
+__device__ __forceinline__ void record_failure(unsigned int* status, volatile int* abort_flag,
+                                               unsigned int bit) {
+  *abort_flag = 1;
+  atomicOr(status, bit);
+}
+
 __device__ __forceinline__ int first_tile() { return blockIdx.x >> 1; }
 __device__ __forceinline__ int tile_stride() { return gridDim.x >> 1; }
 
 // ------------------------------------------------------------ producer
-template <int STAGE>
-__device__ void run_producer(const GemmLaunch& L, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                             volatile int* abort_flag, int rank) {
-  using C = GemmCfg<STAGE>;
-  for (int p = 0; p < L.n_prob; ++p) {
-    ptx::prefetch_tmap(&L.tm_a[p]);
-    ptx::prefetch_tmap(&L.tm_b[p]);
-    if (STAGE != kStageGram) ptx::prefetch_tmap(&L.tm_at[p]);
-    if (STAGE == kStagePoly) ptx::prefetch_tmap(&L.tm_bt[p]);
-  }
+struct ProdState {
   int stage = 0;
   uint32_t phase = 0;
-  uint32_t armed = 0, armed_parity = 0;
-  bool ok = true;
-  const uint32_t leader_full0 = ptx::mapa_shared(ptx::smem_u32(full), 0);
-  for (int t = first_tile(); ok && t < L.total_tiles; t += tile_stride()) {
-    const Tile tl = decode_tile<STAGE>(L, t, rank);
-    const GemmProblem& P = L.prob[tl.prob];
-    const CUtensorMap* ta = &L.tm_a[tl.prob];
-    const CUtensorMap* tb = &L.tm_b[tl.prob];
-    const CUtensorMap* tat = &L.tm_at[tl.prob];
-    const CUtensorMap* tbt = &L.tm_bt[tl.prob];
-    for (int kb = 0; kb < P.k_blocks; ++kb) {
-      // the pair's MMAs (issued by the even CTA) are done with this slot
-      if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
-        record_failure(L, abort_flag, kErrTimeoutProducer);
-        ok = false;
-        break;
-      }
-      uint8_t* sa = smem + stage * C::kStageBytes;
-      uint8_t* sb = sa + C::kABytes;
-      // both CTAs' copies complete on the even CTA's barrier for this slot
-      const uint32_t bar = leader_full0 + stage * 8;
-      if (rank == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
-      // operand A: this CTA's 128 rows x 64 k-columns, or (below the stored
-      // tiles) the 64 x 128 block at the transposed position, MN-major
-      if (a_transposed<STAGE>(tl.tm >> 1, kb)) {
+  uint32_t armed = 0, armed_parity = 0;  // slots with copies issued, and their phase
+};
+
+// Issues the k-blocks of one tile into the ring.  False on a timed-out wait.
+template <int STAGE>
+__device__ bool produce_tile(const TileCtx& T, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                             uint32_t leader_full0, ProdState& ps, volatile int* abort_flag,
+                             int rank) {
+  using C = Cfg;
+  const int tm = 2 * T.pr + rank;  // this CTA's 128-row block
+  for (int kb = 0; kb < T.k_blocks; ++kb) {
+    // the pair's MMAs (issued by the even CTA) are done with this slot
+    if (!ptx::mbar_wait(&empty[ps.stage], ps.phase ^ 1u, abort_flag)) return false;
+    uint8_t* sa = smem + ps.stage * C::kStageBytes;
+    uint8_t* sb = sa + C::kABytes;
+    // both CTAs' copies complete on the even CTA's barrier for this slot
+    const uint32_t bar = leader_full0 + ps.stage * 8;
+    if (rank == 0) ptx::mbar_arrive_expect_tx(&full[ps.stage], 2 * C::kStageBytes);
+    // operand A: this CTA's 128 rows x 64 k-columns, or (below the stored
+    // tiles) the 64 x 128 block at the transposed position, MN-major
+    if (a_transposed<STAGE>(T.pr, kb)) {
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
-          ptx::tma_load_3d_pair(sa + q * (64 * kTileK * 2), tat, tl.tm * kTileM + q * 64,
-                                kb * kTileK, tl.mat, bar);
-      } else {
-        ptx::tma_load_3d_pair(sa, ta, kb * kTileK, tl.tm * kTileM, tl.mat, bar);
-      }
-      if (STAGE >= kStageUpdate) {
-        // operand B = X[k][j], MN-major: this CTA's 128 columns as 2 slabs of
-        // 64 columns x 64 k-rows
+      for (int q = 0; q < 2; ++q)
+        ptx::tma_load_3d_pair(sa + q * (64 * kTileK * 2), T.at, tm * kTileM + q * 64,
+                              kb * kTileK, T.mat, bar);
+    } else {
+      ptx::tma_load_3d_pair(sa, T.a, kb * kTileK, tm * kTileM, T.mat, bar);
+    }
+    if (STAGE >= kStageUpdate) {
+      // operand B = X[k][j], MN-major: this CTA's 128 columns as 2 slabs of
+      // 64 columns x 64 k-rows
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
-          ptx::tma_load_3d_pair(sb + q * (64 * kTileK * 2), tb, tl.tn * C::kBN + rank * 128 + q * 64,
-                                kb * kTileK, tl.mat, bar);
-      } else if (b_transposed<STAGE>(tl.tn, kb)) {
-        // Poly, below the stored tiles: the transposed block, MN-major
+      for (int q = 0; q < 2; ++q)
+        ptx::tma_load_3d_pair(sb + q * (64 * kTileK * 2), T.b, T.tn * C::kBN + rank * 128 + q * 64,
+                              kb * kTileK, T.mat, bar);
+    } else if (b_transposed<STAGE>(T.tn, kb)) {
+      // Poly, below the stored tiles: the transposed block, MN-major
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
-          ptx::tma_load_3d_pair(sb + q * (64 * kTileK * 2), tbt,
-                                tl.tn * C::kBN + rank * kTileM + q * 64, kb * kTileK, tl.mat, bar);
-      } else {
-        // operand B: this CTA's 128 of the tile column's 256 rows, K-major
-        ptx::tma_load_3d_pair(sb, tb, kb * kTileK, tl.tn * C::kBN + rank * kTileM, tl.mat, bar);
-      }
-      armed |= 1u << stage;
-      armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-      if (++stage == C::kStages) {
-        stage = 0;
-        phase ^= 1u;
-      }
+      for (int q = 0; q < 2; ++q)
+        ptx::tma_load_3d_pair(sb + q * (64 * kTileK * 2), T.bt,
+                              T.tn * C::kBN + rank * kTileM + q * 64, kb * kTileK, T.mat, bar);
+    } else {
+      // operand B: this CTA's 128 of the tile column's 256 rows, K-major
+      ptx::tma_load_3d_pair(sb, T.b, kb * kTileK, T.tn * C::kBN + rank * kTileM, T.mat, bar);
+    }
+    ps.armed |= 1u << ps.stage;
+    ps.armed_parity = (ps.armed_parity & ~(1u << ps.stage)) | (ps.phase << ps.stage);
+    if (++ps.stage == C::kStages) {
+      ps.stage = 0;
+      ps.phase ^= 1u;
     }
   }
-  // Before exit: the pair's MMAs have released every armed stage, so its copies
-  // landed and no commit arrival can still be on its way to this CTA.
-  for (int s = 0; s < C::kStages; ++s)
-    if (armed & (1u << s))
-      if (!ptx::mbar_wait(&empty[s], (armed_parity >> s) & 1u, nullptr))
-        record_failure(L, abort_flag, kErrTimeoutDrain);
+  return true;
+}
+
+// Before exit: the pair's MMAs have released every armed stage, so its copies
+// landed and no commit arrival can still be on its way to this CTA.
+__device__ void drain_producer(const ProdState& ps, uint64_t* empty, unsigned int* status,
+                               volatile int* abort_flag) {
+  for (int s = 0; s < Cfg::kStages; ++s)
+    if (ps.armed & (1u << s))
+      if (!ptx::mbar_wait(&empty[s], (ps.armed_parity >> s) & 1u, nullptr))
+        record_failure(status, abort_flag, kErrTimeoutDrain);
 }
 
 // ------------------------------------------------------------ MMA issuer
 // Runs in the even CTA of the pair only.
-template <int STAGE>
-__device__ void run_mma(const GemmLaunch& L, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                        uint64_t* acc_full, uint64_t* acc_empty, uint64_t* drain,
-                        uint32_t tmem_base, volatile int* abort_flag) {
-  using C = GemmCfg<STAGE>;
-  constexpr bool kBmn = (STAGE >= kStageUpdate);
+struct MmaState {
   int stage = 0;
   uint32_t phase = 0;
   int acc = 0;
   uint32_t acc_phase = 0;
-  bool ok = true;
-  for (int t = first_tile(); ok && t < L.total_tiles; t += tile_stride()) {
-    const Tile tl = decode_tile<STAGE>(L, t, 0);
-    const int kblocks = L.prob[tl.prob].k_blocks;
-    // both CTAs' epilogues have drained this accumulator
-    if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
-      record_failure(L, abort_flag, kErrTimeoutMma);
-      break;
-    }
-    ptx::tc_fence_after();
-    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::kBN);
-    for (int kb = 0; kb < kblocks; ++kb) {
-      // (the barrier orders the TMA writes before these MMA reads; no tcgen05
-      // fence is needed here)
-      if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) {
-        record_failure(L, abort_flag, kErrTimeoutMma);
-        ok = false;
-        break;
-      }
-      const uint32_t sa = ptx::smem_u32(smem + stage * C::kStageBytes);
-      const uint32_t sb = sa + C::kABytes;
-      const bool a_mn = a_transposed<STAGE>(tl.tm >> 1, kb);
-      const bool b_mn = kBmn || b_transposed<STAGE>(tl.tn, kb);
-      const uint32_t idesc = ptx::idesc_bf16(2 * kTileM, C::kBN, b_mn, a_mn);
+};
+
+template <int STAGE>
+__device__ bool mma_tile(const TileCtx& T, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                         uint64_t* acc_full, uint64_t* acc_empty, uint32_t tmem_base,
+                         MmaState& ms, volatile int* abort_flag) {
+  using C = Cfg;
+  constexpr bool kBmn = (STAGE >= kStageUpdate);
+  // both CTAs' epilogues have drained this accumulator
+  if (!ptx::mbar_wait(&acc_empty[ms.acc], ms.acc_phase ^ 1u, abort_flag)) return false;
+  ptx::tc_fence_after();
+  const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ms.acc * C::kBN);
+  for (int kb = 0; kb < T.k_blocks; ++kb) {
+    // (the barrier orders the TMA writes before these MMA reads; no tcgen05
+    // fence is needed here)
+    if (!ptx::mbar_wait(&full[ms.stage], ms.phase, abort_flag)) return false;
+    const uint32_t sa = ptx::smem_u32(smem + ms.stage * C::kStageBytes);
+    const uint32_t sb = sa + C::kABytes;
+    const bool a_mn = a_transposed<STAGE>(T.pr, kb);
+    const bool b_mn = kBmn || b_transposed<STAGE>(T.tn, kb);
+    const uint32_t idesc = ptx::idesc_bf16(2 * kTileM, C::kBN, b_mn, a_mn);
 #pragma unroll
-      for (int k = 0; k < kTileK / 16; ++k) {
-        // K-major SW128: 8-row groups 1024 B apart; a K=16 slice is 32 B on.
-        // MN-major SW128: 64-column slabs (64 x 128 B) apart along M or N,
-        // 8-row groups 1024 B apart along K; a K=16 slice is 16 rows = 2048 B on.
-        const uint64_t da = a_mn ? ptx::smem_desc_sw128(sa + k * 2048, 64 * kTileK * 2, 1024)
-                                 : ptx::smem_desc_sw128(sa + k * 32, 16, 1024);
-        const uint64_t db = b_mn ? ptx::smem_desc_sw128(sb + k * 2048, 64 * kTileK * 2, 1024)
-                                 : ptx::smem_desc_sw128(sb + k * 32, 16, 1024);
-        ptx::mma_bf16_pair(d_tmem, da, db, idesc, (kb | k) != 0 ? 1u : 0u);
-      }
-      // frees the slot in both CTAs once these MMAs have read it
-      ptx::mma_commit_pair(&empty[stage]);
-      if (++stage == C::kStages) {
-        stage = 0;
-        phase ^= 1u;
-      }
+    for (int k = 0; k < kTileK / 16; ++k) {
+      // K-major SW128: 8-row groups 1024 B apart; a K=16 slice is 32 B on.
+      // MN-major SW128: 64-column slabs (64 x 128 B) apart along M or N,
+      // 8-row groups 1024 B apart along K; a K=16 slice is 16 rows = 2048 B on.
+      const uint64_t da = a_mn ? ptx::smem_desc_sw128(sa + k * 2048, 64 * kTileK * 2, 1024)
+                               : ptx::smem_desc_sw128(sa + k * 32, 16, 1024);
+      const uint64_t db = b_mn ? ptx::smem_desc_sw128(sb + k * 2048, 64 * kTileK * 2, 1024)
+                               : ptx::smem_desc_sw128(sb + k * 32, 16, 1024);
+      ptx::mma_bf16_pair(d_tmem, da, db, idesc, (kb | k) != 0 ? 1u : 0u);
     }
-    if (!ok) break;
-    ptx::mma_commit_pair(&acc_full[acc]);
-    if (++acc == 2) {
-      acc = 0;
-      acc_phase ^= 1u;
+    // frees the slot in both CTAs once these MMAs have read it
+    ptx::mma_commit_pair(&empty[ms.stage]);
+    if (++ms.stage == C::kStages) {
+      ms.stage = 0;
+      ms.phase ^= 1u;
     }
   }
-  // Every MMA issued by this thread completes before TMEM is released.
+  ptx::mma_commit_pair(&acc_full[ms.acc]);
+  if (++ms.acc == 2) {
+    ms.acc = 0;
+    ms.acc_phase ^= 1u;
+  }
+  return true;
+}
+
+// Every MMA issued by this thread completes before TMEM is released.
+__device__ void drain_mma(uint64_t* drain, unsigned int* status, volatile int* abort_flag) {
   ptx::mma_commit_pair(drain, 1);
-  if (!ptx::mbar_wait(drain, 0, nullptr)) record_failure(L, abort_flag, kErrTimeoutDrain);
+  if (!ptx::mbar_wait(drain, 0, nullptr)) record_failure(status, abort_flag, kErrTimeoutDrain);
 }
 
 // ------------------------------------------------------------ epilogue helpers
@@ -288,38 +265,11 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&b2);
 }
 
-// 32 consecutive bf16 of a row (zero past `valid`), kept packed.
-__device__ __forceinline__ void load_row32(const __nv_bfloat16* src, int valid,
-                                           uint32_t (&w)[16]) {
-  if (valid >= 32) {
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 v = s4[q];
-      w[4 * q + 0] = v.x;
-      w[4 * q + 1] = v.y;
-      w[4 * q + 2] = v.z;
-      w[4 * q + 3] = v.w;
-    }
-  } else {
-    const unsigned short* h = reinterpret_cast<const unsigned short*>(src);
-#pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      const uint32_t lo = (2 * t < valid) ? h[2 * t] : 0u;
-      const uint32_t hi = (2 * t + 1 < valid) ? h[2 * t + 1] : 0u;
-      w[t] = lo | (hi << 16);
-    }
-  }
-}
-
-// Output staging.  Each epilogue warp owns two 4 KB slots used in turn:
-//   [0, 2 KB)  the warp's 32 x 32 block of the output, bf16, 64-byte rows with
-//              the 64-byte swizzle TMA expects (16-byte unit u of row r sits
-//              at unit u ^ ((r >> 1) & 3)), written with 16-byte stores;
-//   [2, 4 KB)  the mirrored block (entry (i, j) at row j, column i), bf16, no
-//              swizzle: lanes hold consecutive i, so its stores are
-//              conflict-free.
-// Both are stored to global memory by one TMA bulk store each.
+// Output staging.  Each epilogue warp owns kSlots 2 KB slots used in turn,
+// each holding the warp's 32 x 32 block of the output, bf16, 64-byte rows with
+// the 64-byte swizzle TMA expects (16-byte unit u of row r sits at unit
+// u ^ ((r >> 1) & 3)), written with 16-byte stores and stored to global memory
+// by one TMA bulk store.  Poly first loads its A block into the slot by TMA.
 __device__ __forceinline__ uint32_t sw64(int r, int c) {
   return static_cast<uint32_t>(r * 64 + ((((c >> 3) ^ (r >> 1)) & 3) << 4) + (c & 7) * 2);
 }
@@ -338,185 +288,184 @@ __device__ __forceinline__ void stage_row_sw64(uint8_t* blk, int r, const float 
 // ------------------------------------------------------------ epilogue warps
 // Warp w (2..5) owns TMEM lanes 32*(w&3).. (32 rows of the 128-row tile) and
 // walks the tile's 256 columns in 8 chunks of 32.
+struct EpiState {
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  int slot = 0;         // next staging slot (ring of kSlots)
+  uint32_t in_par = 0;  // Poly: parity of each slot's next input load
+};
+
+// One tile.  `dep`/`dep_target` (Poly in the rounds kernel): the counter the
+// A blocks of the b A term wait for before lane 0 loads them.  False on a
+// timed-out wait.
 template <int STAGE>
-__device__ void run_epilogue(const GemmLaunch& L, uint64_t* acc_full, uint64_t* acc_empty,
-                             uint64_t* in_bar, uint32_t tmem_base, uint8_t* staging,
-                             volatile int* abort_flag, int warp, int lane, int rank) {
-  using C = GemmCfg<STAGE>;
+__device__ bool epilogue_tile(const TileCtx& T, const GemmScalars& k, uint64_t* acc_full,
+                              uint64_t* acc_empty, uint64_t* my_in, uint8_t* my_slots,
+                              uint32_t tmem_base, EpiState& es, volatile int* abort_flag,
+                              int quarter, int lane, int rank, const unsigned int* dep,
+                              unsigned int dep_target) {
+  using C = Cfg;
   constexpr int kChunks = C::kBN / 32;
   constexpr bool kSym = STAGE <= kStagePoly;
   constexpr bool kPoly = STAGE == kStagePoly;
-  const int quarter = warp & 3;
-  uint8_t* my_slots = staging + quarter * C::kSlots * C::kSlotBytes;
-  uint64_t* my_in = in_bar + quarter * C::kSlots;
-  int acc = 0;
-  uint32_t acc_phase = 0;
-  int slot = 0;             // next staging slot (ring of kSlots)
-  uint32_t in_par = 0;      // Poly: parity of each slot's next input load
-  for (int t = first_tile(); t < L.total_tiles; t += tile_stride()) {
-    __syncwarp();
-    const Tile tl = decode_tile<STAGE>(L, t, rank);
-    const GemmProblem& P = L.prob[tl.prob];
-    const CUtensorMap* tm_out = &L.tm_out[tl.prob];
-    const CUtensorMap* tm_in = &L.tm_in[tl.prob];
-    float s = 1.f;
-    if (STAGE != kStagePoly && P.first_round)
-      s = inv_fro_norm(P.parts + static_cast<size_t>(tl.mat) * P.nparts, P.nparts, L.eps, lane);
-    const int i0 = tl.tm * kTileM + quarter * 32;  // first row of this warp
-    const int ncols = kSym ? P.m : P.n;
-    const int jt = tl.tn * C::kBN;
-    // live chunks: c_lo <= ch < c_hi (rows in range, columns in range)
-    const int c_lo = 0;
-    const int c_hi = i0 < P.m ? min(kChunks, (ncols - jt + 31) / 32) : 0;
-    // Poly: the first two live chunks' A blocks into their slots
-    if constexpr (kPoly) {
-      if (lane == 0) {
-        for (int k = 0; k < 2 && c_lo + k < c_hi; ++k) {
-          const int sl = (slot + k) % C::kSlots;
-          if (k == 0) ptx::bulk_wait_read<2>(); else ptx::bulk_wait_read<1>();
-          ptx::mbar_arrive_expect_tx(&my_in[sl], 2048);
-          ptx::tma_load_3d(my_slots + sl * C::kSlotBytes, tm_in, jt + 32 * (c_lo + k), i0, tl.mat,
-                           &my_in[sl]);
-        }
-      }
-      __syncwarp();
-    }
-
-    const bool got = ptx::mbar_wait(&acc_full[acc], acc_phase, abort_flag);
-    __syncwarp();
-    if (!got) {
-      record_failure(L, abort_flag, kErrTimeoutEpilogue);
-      break;
-    }
-    ptx::tc_fence_after();
-    const uint32_t tbase =
-        tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * C::kBN);
-    bool failed = false;
-#pragma unroll 1
-    for (int ch = c_lo; ch < c_hi; ++ch) {
-      const int j0 = jt + ch * 32;
-      uint8_t* blk = my_slots + slot * C::kSlotBytes;
-      uint32_t ev[16];
-      if constexpr (kPoly) {
-        const uint32_t par = (in_par >> slot) & 1u;
-        if (!ptx::mbar_wait(&my_in[slot], par, abort_flag)) failed = true;
-        in_par ^= 1u << slot;
-        __syncwarp();
-        // row `lane` of the A block, 64-byte swizzled like the output blocks
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 w = *reinterpret_cast<const uint4*>(blk + sw64(lane, 8 * q));
-          ev[4 * q + 0] = w.x;
-          ev[4 * q + 1] = w.y;
-          ev[4 * q + 2] = w.z;
-          ev[4 * q + 3] = w.w;
-        }
-      } else {
-        // the slot's previous bulk store (two chunks ago) has read its data
-        if (lane == 0) ptx::bulk_wait_read<1>();
-      }
-      __syncwarp();
-      uint32_t v[32];
-      ptx::tmem_ld32(tbase + static_cast<uint32_t>(ch * 32), v);
-      ptx::tmem_ld_wait();
-      float val[32];
-      if constexpr (STAGE == kStageGram) {
-#pragma unroll
-        for (int q = 0; q < 32; ++q) val[q] = __uint_as_float(v[q]) * (s * s);
-      } else if constexpr (kPoly) {
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          val[2 * q] = fmaf(L.c, __uint_as_float(v[2 * q]), L.b * bf_lo(ev[q]));
-          val[2 * q + 1] = fmaf(L.c, __uint_as_float(v[2 * q + 1]), L.b * bf_hi(ev[q]));
-        }
-        // B' = a I + b A + c A A: the update then needs no a X term
-        if (j0 == i0) {
-#pragma unroll
-          for (int q = 0; q < 32; ++q) val[q] += (q == lane) ? L.a : 0.f;
-        }
-      } else {
-#pragma unroll
-        for (int q = 0; q < 32; ++q) val[q] = s * __uint_as_float(v[q]);
-      }
-
-      stage_row_sw64(blk, lane, val);
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        ptx::tma_store_3d(tm_out, j0, i0, tl.mat, blk);
-        ptx::bulk_commit();
-        // Poly: the A block two live chunks ahead goes into the slot whose
-        // store was issued one chunk ago
-        if (kPoly && ch + 2 < c_hi) {
-          const int sl = (slot + 2) % C::kSlots;
-          ptx::bulk_wait_read<1>();
-          ptx::mbar_arrive_expect_tx(&my_in[sl], 2048);
-          ptx::tma_load_3d(my_slots + sl * C::kSlotBytes, tm_in, j0 + 64, i0, tl.mat, &my_in[sl]);
-        }
-      }
-      slot = (slot + 1) % C::kSlots;
-    }
-    ptx::tc_fence_before();
-    __syncwarp();
-    // release the accumulator on the even CTA's barrier (the MMA issuer's)
-    if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&acc_empty[acc]), 0));
-    if (++acc == 2) {
-      acc = 0;
-      acc_phase ^= 1u;
-    }
-    if (failed) {
-      record_failure(L, abort_flag, kErrTimeoutEpilogue);
-      break;
-    }
-  }
-  // all bulk copies of this warp are complete before the CTA exits
-  if (lane == 0) ptx::bulk_wait<0>();
   __syncwarp();
+  float s = 1.f;
+  if (STAGE != kStagePoly && T.first_round)
+    s = inv_fro_norm(T.parts + static_cast<size_t>(T.mat) * T.nparts, T.nparts, k.eps, lane);
+  const int tm = 2 * T.pr + rank;
+  const int i0 = tm * kTileM + quarter * 32;  // first row of this warp
+  const int ncols = kSym ? T.m : T.n;
+  const int jt = T.tn * C::kBN;
+  // live chunks: c_lo <= ch < c_hi (rows in range, columns in range)
+  const int c_lo = 0;
+  const int c_hi = i0 < T.m ? min(kChunks, (ncols - jt + 31) / 32) : 0;
+  // Poly: the first two live chunks' A blocks into their slots
+  if constexpr (kPoly) {
+    int ok = 1;
+    if (lane == 0) {
+      if (dep != nullptr && c_hi > c_lo) {
+        if (!ptx::wait_counter(dep, dep_target, abort_flag)) ok = 0;
+        ptx::fence_proxy_async_global();
+      }
+      for (int q = 0; ok && q < 2 && c_lo + q < c_hi; ++q) {
+        const int sl = (es.slot + q) % C::kSlots;
+        if (q == 0) ptx::bulk_wait_read<2>(); else ptx::bulk_wait_read<1>();
+        ptx::mbar_arrive_expect_tx(&my_in[sl], 2048);
+        ptx::tma_load_3d(my_slots + sl * C::kSlotBytes, T.in, jt + 32 * (c_lo + q), i0, T.mat,
+                         &my_in[sl]);
+      }
+    }
+    if (__shfl_sync(0xffffffffu, ok, 0) == 0) return false;
+  }
+
+  const bool got = ptx::mbar_wait(&acc_full[es.acc], es.acc_phase, abort_flag);
+  __syncwarp();
+  if (!got) return false;
+  ptx::tc_fence_after();
+  const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                         static_cast<uint32_t>(es.acc * C::kBN);
+  bool failed = false;
+#pragma unroll 1
+  for (int ch = c_lo; ch < c_hi; ++ch) {
+    const int j0 = jt + ch * 32;
+    uint8_t* blk = my_slots + es.slot * C::kSlotBytes;
+    uint32_t ev[16];
+    if constexpr (kPoly) {
+      const uint32_t par = (es.in_par >> es.slot) & 1u;
+      if (!ptx::mbar_wait(&my_in[es.slot], par, abort_flag)) failed = true;
+      es.in_par ^= 1u << es.slot;
+      __syncwarp();
+      // row `lane` of the A block, 64-byte swizzled like the output blocks
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w = *reinterpret_cast<const uint4*>(blk + sw64(lane, 8 * q));
+        ev[4 * q + 0] = w.x;
+        ev[4 * q + 1] = w.y;
+        ev[4 * q + 2] = w.z;
+        ev[4 * q + 3] = w.w;
+      }
+    } else {
+      // the slot's previous bulk store (kSlots - 1 chunks ago) has read its data
+      if (lane == 0) ptx::bulk_wait_read<C::kSlots - 1>();
+    }
+    __syncwarp();
+    uint32_t v[32];
+    ptx::tmem_ld32(tbase + static_cast<uint32_t>(ch * 32), v);
+    ptx::tmem_ld_wait();
+    float val[32];
+    if constexpr (STAGE == kStageGram) {
+#pragma unroll
+      for (int q = 0; q < 32; ++q) val[q] = __uint_as_float(v[q]) * (s * s);
+    } else if constexpr (kPoly) {
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        val[2 * q] = fmaf(k.c, __uint_as_float(v[2 * q]), k.b * bf_lo(ev[q]));
+        val[2 * q + 1] = fmaf(k.c, __uint_as_float(v[2 * q + 1]), k.b * bf_hi(ev[q]));
+      }
+      // B' = a I + b A + c A A: the update then needs no a X term
+      if (j0 == i0) {
+#pragma unroll
+        for (int q = 0; q < 32; ++q) val[q] += (q == lane) ? k.a : 0.f;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 32; ++q) val[q] = s * __uint_as_float(v[q]);
+    }
+    stage_row_sw64(blk, lane, val);
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      ptx::tma_store_3d(T.out, j0, i0, T.mat, blk);
+      ptx::bulk_commit();
+      // Poly: the A block two live chunks ahead goes into the slot whose
+      // store was issued one chunk ago
+      if (kPoly && ch + 2 < c_hi) {
+        const int sl = (es.slot + 2) % C::kSlots;
+        ptx::bulk_wait_read<1>();
+        ptx::mbar_arrive_expect_tx(&my_in[sl], 2048);
+        ptx::tma_load_3d(my_slots + sl * C::kSlotBytes, T.in, j0 + 64, i0, T.mat, &my_in[sl]);
+      }
+    }
+    es.slot = (es.slot + 1) % C::kSlots;
+  }
+  ptx::tc_fence_before();
+  __syncwarp();
+  // release the accumulator on the even CTA's barrier (the MMA issuer's)
+  if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&acc_empty[es.acc]), 0));
+  if (++es.acc == 2) {
+    es.acc = 0;
+    es.acc_phase ^= 1u;
+  }
+  return !failed;
 }
 
-// ------------------------------------------------------------ kernel
-template <int STAGE>
-__global__ void __launch_bounds__(GemmCfg<STAGE>::kThreads, 1)
-    ns_gemm_kernel(const __grid_constant__ GemmLaunch L) {
-  using C = GemmCfg<STAGE>;
-  extern __shared__ uint8_t smem_raw[];
+// ------------------------------------------------------------ common setup
+struct Smem {
+  uint8_t* ring;
+  uint8_t* staging;
+  uint64_t *full, *empty, *acc_full, *acc_empty, *drain, *in_bar;
+  uint32_t* tmem_slot;
+  volatile int* abort_flag;
+};
+
+__device__ __forceinline__ Smem carve_smem(uint8_t* smem_raw) {
+  using C = Cfg;
+  Smem m;
   // both CTAs of the pair get the same aligned offsets (the pair MMA reads both)
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
+  m.ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* staging = smem + C::kStages * C::kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + C::kStagingBytes);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + C::kStages;
-  uint64_t* acc_full = bars + 2 * C::kStages;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* drain = acc_empty + 2;
-  uint64_t* in_bar = drain + 1;  // Poly: one per epilogue warp and slot
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(in_bar + C::kEpiWarps * C::kSlots);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  m.staging = m.ring + C::kStages * C::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(m.staging + C::kStagingBytes);
+  m.full = bars;
+  m.empty = bars + C::kStages;
+  m.acc_full = bars + 2 * C::kStages;
+  m.acc_empty = m.acc_full + 2;
+  m.drain = m.acc_empty + 2;
+  m.in_bar = m.drain + 1;  // Poly: one per epilogue warp and slot
+  m.tmem_slot = reinterpret_cast<uint32_t*>(m.in_bar + C::kEpiWarps * C::kSlots);
+  m.abort_flag = reinterpret_cast<volatile int*>(m.tmem_slot + 1);
+  return m;
+}
 
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int rank = static_cast<int>(ptx::cluster_ctarank());
-  // the next stage may be scheduled now; it takes an SM only once this CTA has
-  // left it, and waits for this grid to finish before reading its output
-  ptx::griddep_launch_dependents();
-
+// Barriers, TMEM; returns the TMEM base.  Called by every thread of both CTAs.
+__device__ __forceinline__ uint32_t setup_cta(const Smem& m, int warp) {
+  using C = Cfg;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      ptx::mbar_init(&full[s], 1);   // the even CTA's expect_tx (+ both CTAs' bytes)
-      ptx::mbar_init(&empty[s], 1);  // the pair MMA commit
+      ptx::mbar_init(&m.full[s], 1);   // the even CTA's expect_tx (+ both CTAs' bytes)
+      ptx::mbar_init(&m.empty[s], 1);  // the pair MMA commit
     }
     for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(&acc_full[s], 1);
-      ptx::mbar_init(&acc_empty[s], 2 * C::kEpiWarps);  // both CTAs' epilogue warps
+      ptx::mbar_init(&m.acc_full[s], 1);
+      ptx::mbar_init(&m.acc_empty[s], 2 * C::kEpiWarps);  // both CTAs' epilogue warps
     }
-    ptx::mbar_init(drain, 1);
-    for (int k = 0; k < C::kEpiWarps * C::kSlots; ++k) ptx::mbar_init(&in_bar[k], 1);
-    *abort_flag = 0;
+    ptx::mbar_init(m.drain, 1);
+    for (int k = 0; k < C::kEpiWarps * C::kSlots; ++k) ptx::mbar_init(&m.in_bar[k], 1);
+    *m.abort_flag = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc_pair(tmem_slot, C::kTmemCols);
+    ptx::tmem_alloc_pair(m.tmem_slot, C::kTmemCols);
     ptx::tmem_relinquish_pair();
   }
   __syncwarp();
@@ -524,20 +473,10 @@ __global__ void __launch_bounds__(GemmCfg<STAGE>::kThreads, 1)
   // both CTAs' barriers exist before either's copies signal the other's
   ptx::cluster_sync();
   ptx::tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  // setup above overlapped the previous stage's tail; its output is read below
-  ptx::griddep_wait();
+  return *m.tmem_slot;
+}
 
-  if (warp == 0) {
-    if (lane == 0) run_producer<STAGE>(L, smem, full, empty, abort_flag, rank);
-  } else if (warp == 1) {
-    if (lane == 0 && rank == 0)
-      run_mma<STAGE>(L, smem, full, empty, acc_full, acc_empty, drain, tmem_base, abort_flag);
-  } else {
-    run_epilogue<STAGE>(L, acc_full, acc_empty, in_bar, tmem_base, staging, abort_flag, warp,
-                        lane, rank);
-  }
-
+__device__ __forceinline__ void teardown_cta(uint32_t tmem_base, int warp) {
   __syncwarp();
   ptx::tc_fence_before();
   // neither CTA exits while the other may still write into its shared memory
@@ -545,8 +484,352 @@ __global__ void __launch_bounds__(GemmCfg<STAGE>::kThreads, 1)
   ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    ptx::tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
   }
+}
+
+// ============================================================ staged kernel
+struct Tile {
+  int prob, mat, pr, tn;
+};
+
+// Linear pair-tile index -> (problem, matrix, pair row, tile col).
+// Symmetric stages enumerate, per pair row p, the tile columns tn >= p.
+template <int STAGE>
+__device__ __forceinline__ Tile decode_tile(const GemmLaunch& L, int t) {
+  int p = 0;
+#pragma unroll 1
+  while (p + 1 < L.n_prob && t >= L.prob[p + 1].tile_begin) ++p;
+  const GemmProblem& P = L.prob[p];
+  const int local = t - P.tile_begin;
+  Tile r;
+  r.prob = p;
+  r.mat = local / P.tiles_per_mat;
+  int w = local - r.mat * P.tiles_per_mat;
+  if (P.reverse) r.mat = P.batch - 1 - r.mat;
+  r.pr = P.tiles_m;  // out of range unless found (no stores then)
+  r.tn = 0;
+  if (STAGE >= kStageUpdate) {
+    r.pr = w / P.tiles_n;
+    r.tn = w - r.pr * P.tiles_n;
+  } else {
+#pragma unroll 1
+    for (int q = 0; q < P.tiles_m; ++q) {
+      const int cnt = P.tiles_n - q;
+      if (w < cnt) {
+        r.pr = q;
+        r.tn = q + w;
+        break;
+      }
+      w -= cnt;
+    }
+  }
+  return r;
+}
+
+__device__ __forceinline__ TileCtx staged_ctx(const GemmLaunch& L, const Tile& tl) {
+  const GemmProblem& P = L.prob[tl.prob];
+  TileCtx T;
+  T.a = &L.tm_a[tl.prob];
+  T.at = &L.tm_at[tl.prob];
+  T.b = &L.tm_b[tl.prob];
+  T.bt = &L.tm_bt[tl.prob];
+  T.out = &L.tm_out[tl.prob];
+  T.in = &L.tm_in[tl.prob];
+  T.mat = tl.mat;
+  T.pr = tl.pr;
+  T.tn = tl.tn;
+  T.m = P.m;
+  T.n = P.n;
+  T.k_blocks = P.k_blocks;
+  T.parts = P.parts;
+  T.nparts = P.nparts;
+  T.first_round = P.first_round;
+  return T;
+}
+
+template <int STAGE>
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
+    ns_gemm_kernel(const __grid_constant__ GemmLaunch L) {
+  extern __shared__ uint8_t smem_raw[];
+  const Smem sm = carve_smem(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(ptx::cluster_ctarank());
+  // the next stage may be scheduled now; it takes an SM only once this CTA has
+  // left it, and waits for this grid to finish before reading its output
+  ptx::griddep_launch_dependents();
+  const uint32_t tmem_base = setup_cta(sm, warp);
+  // setup above overlapped the previous stage's tail; its output is read below
+  ptx::griddep_wait();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int p = 0; p < L.n_prob; ++p) {
+        ptx::prefetch_tmap(&L.tm_a[p]);
+        ptx::prefetch_tmap(&L.tm_b[p]);
+        if (STAGE != kStageGram) ptx::prefetch_tmap(&L.tm_at[p]);
+        if (STAGE == kStagePoly) ptx::prefetch_tmap(&L.tm_bt[p]);
+      }
+      ProdState ps;
+      const uint32_t leader_full0 = ptx::mapa_shared(ptx::smem_u32(sm.full), 0);
+      for (int t = first_tile(); t < L.total_tiles; t += tile_stride()) {
+        const TileCtx T = staged_ctx(L, decode_tile<STAGE>(L, t));
+        if (!produce_tile<STAGE>(T, sm.ring, sm.full, sm.empty, leader_full0, ps,
+                                 sm.abort_flag, rank)) {
+          record_failure(L.status, sm.abort_flag, kErrTimeoutProducer);
+          break;
+        }
+      }
+      drain_producer(ps, sm.empty, L.status, sm.abort_flag);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      MmaState ms;
+      for (int t = first_tile(); t < L.total_tiles; t += tile_stride()) {
+        const TileCtx T = staged_ctx(L, decode_tile<STAGE>(L, t));
+        if (!mma_tile<STAGE>(T, sm.ring, sm.full, sm.empty, sm.acc_full, sm.acc_empty, tmem_base,
+                             ms, sm.abort_flag)) {
+          record_failure(L.status, sm.abort_flag, kErrTimeoutMma);
+          break;
+        }
+      }
+      drain_mma(sm.drain, L.status, sm.abort_flag);
+    }
+  } else {
+    const int quarter = warp & 3;
+    uint8_t* my_slots = sm.staging + quarter * Cfg::kSlots * Cfg::kSlotBytes;
+    uint64_t* my_in = sm.in_bar + quarter * Cfg::kSlots;
+    const GemmScalars k{L.a, L.b, L.c, L.eps};
+    EpiState es;
+    for (int t = first_tile(); t < L.total_tiles; t += tile_stride()) {
+      const TileCtx T = staged_ctx(L, decode_tile<STAGE>(L, t));
+      if (!epilogue_tile<STAGE>(T, k, sm.acc_full, sm.acc_empty, my_in, my_slots, tmem_base, es,
+                                sm.abort_flag, quarter, lane, rank, nullptr, 0u)) {
+        record_failure(L.status, sm.abort_flag, kErrTimeoutEpilogue);
+        break;
+      }
+    }
+    // all bulk copies of this warp are complete before the CTA exits
+    if (lane == 0) ptx::bulk_wait<0>();
+    __syncwarp();
+  }
+  teardown_cta(tmem_base, warp);
+}
+
+// ============================================================ rounds kernel
+struct Item {
+  int r, s, p, mat, pr, tn;
+};
+
+// Linear item index -> (round, stage, problem, matrix, pair row, tile col).
+__device__ __forceinline__ Item decode_item(const RoundsLaunch& L, int item) {
+  Item it;
+  it.r = item / L.round_tiles;
+  int w = item - it.r * L.round_tiles;
+  int s = 0;
+  while (s < 2 && w >= L.stage_tiles[s]) {
+    w -= L.stage_tiles[s];
+    ++s;
+  }
+  int p = 0;
+#pragma unroll 1
+  while (p + 1 < L.n_prob && w >= L.prob[p + 1].tile_begin[s]) ++p;
+  const RoundsProblem& P = L.prob[p];
+  const int local = w - P.tile_begin[s];
+  it.s = s;
+  it.p = p;
+  it.mat = local / P.tiles_per_mat[s];
+  int q = local - it.mat * P.tiles_per_mat[s];
+  it.pr = P.tiles_m;
+  it.tn = 0;
+  if (s == kStageUpdate) {
+    it.pr = q / P.tiles_n[s];
+    it.tn = q - it.pr * P.tiles_n[s];
+  } else {
+#pragma unroll 1
+    for (int row = 0; row < P.tiles_m; ++row) {
+      const int cnt = P.tiles_n[s] - row;
+      if (q < cnt) {
+        it.pr = row;
+        it.tn = row + q;
+        break;
+      }
+      q -= cnt;
+    }
+  }
+  return it;
+}
+
+// Completion-counter value that every tile of the stages before `it` (for its
+// matrix) has stored.
+__device__ __forceinline__ unsigned int dep_target(const RoundsLaunch& L, const Item& it) {
+  const RoundsProblem& P = L.prob[it.p];
+  const unsigned int per_round = static_cast<unsigned int>(
+      P.tiles_per_mat[0] + P.tiles_per_mat[1] + P.tiles_per_mat[2]);
+  unsigned int tiles = static_cast<unsigned int>(it.r) * per_round;
+  if (it.s >= 1) tiles += P.tiles_per_mat[0];
+  if (it.s >= 2) tiles += P.tiles_per_mat[1];
+  return tiles * Cfg::kSignalsPerTile;
+}
+
+__device__ __forceinline__ TileCtx rounds_ctx(const RoundsLaunch& L, const Item& it) {
+  const RoundsProblem& P = L.prob[it.p];
+  const int cur = it.r & 1;
+  TileCtx T;
+  if (it.s == kStageGram) {          // A = s^2 X X^T
+    T.a = &L.x_op[it.p][cur];
+    T.at = nullptr;
+    T.b = &L.x_op[it.p][cur];
+    T.bt = nullptr;
+    T.out = &L.a_blk[it.p];
+    T.in = nullptr;
+  } else if (it.s == kStagePoly) {   // B' = a I + b A + c A A
+    T.a = &L.a_op[it.p];
+    T.at = &L.a_mn[it.p];
+    T.b = &L.a_op[it.p];
+    T.bt = &L.a_mn[it.p];
+    T.out = &L.b_out[it.p];
+    T.in = &L.a_blk[it.p];
+  } else {                           // X' = s B' X
+    T.a = &L.b_op[it.p];
+    T.at = &L.b_mn[it.p];
+    T.b = &L.x_mn[it.p][cur];
+    T.bt = nullptr;
+    T.out = &L.x_out[it.p][cur ^ 1];
+    T.in = nullptr;
+  }
+  T.mat = it.mat;
+  T.pr = it.pr;
+  T.tn = it.tn;
+  T.m = P.m;
+  T.n = P.n;
+  T.k_blocks = P.k_blocks[it.s];
+  T.parts = P.parts;
+  T.nparts = P.nparts;
+  T.first_round = it.r == 0 ? 1 : 0;
+  return T;
+}
+
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
+    ns_rounds_kernel(const __grid_constant__ RoundsLaunch L) {
+  extern __shared__ uint8_t smem_raw[];
+  const Smem sm = carve_smem(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(ptx::cluster_ctarank());
+  ptx::griddep_launch_dependents();
+  const uint32_t tmem_base = setup_cta(sm, warp);
+  // X0, the norm partials and the zeroed counters come from the prologue
+  ptx::griddep_wait();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int p = 0; p < L.n_prob; ++p) {
+        ptx::prefetch_tmap(&L.x_op[p][0]);
+        ptx::prefetch_tmap(&L.x_op[p][1]);
+        ptx::prefetch_tmap(&L.x_mn[p][0]);
+        ptx::prefetch_tmap(&L.x_mn[p][1]);
+        ptx::prefetch_tmap(&L.a_op[p]);
+        ptx::prefetch_tmap(&L.a_mn[p]);
+        ptx::prefetch_tmap(&L.b_op[p]);
+        ptx::prefetch_tmap(&L.b_mn[p]);
+      }
+      ProdState ps;
+      const uint32_t leader_full0 = ptx::mapa_shared(ptx::smem_u32(sm.full), 0);
+      for (int i = first_tile(); i < L.total_items; i += tile_stride()) {
+        const Item it = decode_item(L, i);
+        // the operands of this tile are the stored outputs of the stages before
+        const unsigned int target = dep_target(L, it);
+        if (target > 0) {
+          if (!ptx::wait_counter(L.done + L.prob[it.p].done_begin + it.mat, target,
+                                 sm.abort_flag)) {
+            record_failure(L.status, sm.abort_flag, kErrTimeoutDepend);
+            break;
+          }
+          ptx::fence_proxy_async_global();
+        }
+        const TileCtx T = rounds_ctx(L, it);
+        bool ok;
+        if (it.s == kStageGram)
+          ok = produce_tile<kStageGram>(T, sm.ring, sm.full, sm.empty, leader_full0, ps,
+                                        sm.abort_flag, rank);
+        else if (it.s == kStagePoly)
+          ok = produce_tile<kStagePoly>(T, sm.ring, sm.full, sm.empty, leader_full0, ps,
+                                        sm.abort_flag, rank);
+        else
+          ok = produce_tile<kStageUpdate>(T, sm.ring, sm.full, sm.empty, leader_full0, ps,
+                                          sm.abort_flag, rank);
+        if (!ok) {
+          record_failure(L.status, sm.abort_flag, kErrTimeoutProducer);
+          break;
+        }
+      }
+      drain_producer(ps, sm.empty, L.status, sm.abort_flag);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      MmaState ms;
+      for (int i = first_tile(); i < L.total_items; i += tile_stride()) {
+        const Item it = decode_item(L, i);
+        const TileCtx T = rounds_ctx(L, it);
+        bool ok;
+        if (it.s == kStageGram)
+          ok = mma_tile<kStageGram>(T, sm.ring, sm.full, sm.empty, sm.acc_full, sm.acc_empty,
+                                    tmem_base, ms, sm.abort_flag);
+        else if (it.s == kStagePoly)
+          ok = mma_tile<kStagePoly>(T, sm.ring, sm.full, sm.empty, sm.acc_full, sm.acc_empty,
+                                    tmem_base, ms, sm.abort_flag);
+        else
+          ok = mma_tile<kStageUpdate>(T, sm.ring, sm.full, sm.empty, sm.acc_full, sm.acc_empty,
+                                      tmem_base, ms, sm.abort_flag);
+        if (!ok) {
+          record_failure(L.status, sm.abort_flag, kErrTimeoutMma);
+          break;
+        }
+      }
+      drain_mma(sm.drain, L.status, sm.abort_flag);
+    }
+  } else {
+    const int quarter = warp & 3;
+    uint8_t* my_slots = sm.staging + quarter * Cfg::kSlots * Cfg::kSlotBytes;
+    uint64_t* my_in = sm.in_bar + quarter * Cfg::kSlots;
+    const GemmScalars k{L.a, L.b, L.c, L.eps};
+    EpiState es;
+    for (int i = first_tile(); i < L.total_items; i += tile_stride()) {
+      const Item it = decode_item(L, i);
+      const TileCtx T = rounds_ctx(L, it);
+      unsigned int* ctr = L.done + L.prob[it.p].done_begin + it.mat;
+      bool ok;
+      if (it.s == kStageGram)
+        ok = epilogue_tile<kStageGram>(T, k, sm.acc_full, sm.acc_empty, my_in, my_slots,
+                                       tmem_base, es, sm.abort_flag, quarter, lane, rank,
+                                       nullptr, 0u);
+      else if (it.s == kStagePoly)
+        ok = epilogue_tile<kStagePoly>(T, k, sm.acc_full, sm.acc_empty, my_in, my_slots,
+                                       tmem_base, es, sm.abort_flag, quarter, lane, rank, ctr,
+                                       dep_target(L, it));
+      else
+        ok = epilogue_tile<kStageUpdate>(T, k, sm.acc_full, sm.acc_empty, my_in, my_slots,
+                                         tmem_base, es, sm.abort_flag, quarter, lane, rank,
+                                         nullptr, 0u);
+      if (!ok) {
+        record_failure(L.status, sm.abort_flag, kErrTimeoutEpilogue);
+        break;
+      }
+      // this warp's blocks of the tile are in global memory: count them
+      if (lane == 0) {
+        ptx::bulk_wait<0>();
+        ptx::fence_proxy_async_global();
+        ptx::red_release_gpu_add(ctr, 1u);
+      }
+      __syncwarp();
+    }
+    // all bulk copies of this warp are complete before the CTA exits
+    if (lane == 0) ptx::bulk_wait<0>();
+    __syncwarp();
+  }
+  teardown_cta(tmem_base, warp);
 }
 
 // ------------------------------------------------------------ wait self-test
@@ -572,13 +855,40 @@ cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_
 }
 
 // ------------------------------------------------------------ launchers
-template <int STAGE>
-static cudaError_t launch_instance(const GemmLaunch& l, int pair_tiles, int sms, cudaStream_t s) {
-  constexpr int kSmem = GemmCfg<STAGE>::kSmem;
-  static int max_clusters[64] = {0};
+// Clusters that fit on the device at once (one CTA per SM), queried once per
+// device and kernel.
+template <typename K>
+static cudaError_t max_clusters(K kernel, int slot, int sms, int* out) {
+  static int cache[4][64] = {{0}};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (cache[slot][dev] == 0) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(2 * (sms / 2));
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    cache[slot][dev] = n < 1 ? 1 : n;
+  }
+  *out = cache[slot][dev];
+  return cudaSuccess;
+}
+
+template <typename K, typename P>
+static cudaError_t launch_pairs(K kernel, const P& params, int clusters, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -587,30 +897,24 @@ static cudaError_t launch_instance(const GemmLaunch& l, int pair_tiles, int sms,
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.blockDim = dim3(GemmCfg<STAGE>::kThreads);
-  cfg.dynamicSmemBytes = kSmem;
+  cfg.blockDim = dim3(Cfg::kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmem;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;  // occupancy query: cluster shape only
-  // clusters that fit on the device at once (one CTA per SM), queried once
-  int n = dev < 64 ? max_clusters[dev] : 0;
-  if (n == 0) {
-    e = cudaFuncSetAttribute(ns_gemm_kernel<STAGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmem);
-    if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(2 * (sms / 2));
-    e = cudaOccupancyMaxActiveClusters(&n, ns_gemm_kernel<STAGE>, &cfg);
-    if (e != cudaSuccess) return e;
-    if (n < 1) n = 1;
-    if (dev < 64) max_clusters[dev] = n;
-  }
-  const int clusters = pair_tiles < n ? pair_tiles : n;
-  cfg.gridDim = dim3(2 * clusters);
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, ns_gemm_kernel<STAGE>, l);
+  cfg.gridDim = dim3(2 * clusters);
+  return cudaLaunchKernelEx(&cfg, kernel, params);
 }
 
-int gemm_smem_bytes() { return GemmCfg<kStageUpdate>::kSmem; }
+template <int STAGE>
+static cudaError_t launch_instance(const GemmLaunch& l, int pair_tiles, int sms, cudaStream_t s) {
+  int n = 0;
+  const cudaError_t e = max_clusters(ns_gemm_kernel<STAGE>, STAGE, sms, &n);
+  if (e != cudaSuccess) return e;
+  return launch_pairs(ns_gemm_kernel<STAGE>, l, pair_tiles < n ? pair_tiles : n, s);
+}
+
+int gemm_smem_bytes() { return Cfg::kSmem; }
 
 cudaError_t launch_gemm(const GemmLaunch& l, int stage, int pair_tiles, int sms, cudaStream_t s) {
   switch (stage) {
@@ -623,6 +927,15 @@ cudaError_t launch_gemm(const GemmLaunch& l, int stage, int pair_tiles, int sms,
     default:
       return cudaErrorInvalidValue;
   }
+}
+
+// Every cluster of the grid must be resident at once: tiles wait for tiles of
+// other clusters.  The grid is therefore never larger than what fits.
+cudaError_t launch_rounds(const RoundsLaunch& l, int sms, cudaStream_t s) {
+  int n = 0;
+  const cudaError_t e = max_clusters(ns_rounds_kernel, 3, sms, &n);
+  if (e != cudaSuccess) return e;
+  return launch_pairs(ns_rounds_kernel, l, l.total_items < n ? l.total_items : n, s);
 }
 
 }  // namespace muon

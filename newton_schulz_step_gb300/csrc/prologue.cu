@@ -101,6 +101,10 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
   __shared__ float red[8];
   // the first Gram stage may be scheduled once every block here has started
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // completion counters of the persistent rounds kernel, which reads them only
+  // after this grid has completed
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < L.n_zero; i += blockDim.x) L.zero[i] = 0u;
   int gi = 0;
   while (gi + 1 < L.n_groups && static_cast<int>(blockIdx.x) >= L.grp[gi + 1].block_begin) ++gi;
   const PrologueGroup& A = L.grp[gi];

@@ -57,15 +57,20 @@ def test_workspace_bytes(lib):
     assert lib.muon_workspace_bytes(1, 70000, 7) == 0
     # small path: fp32 m x n per matrix
     assert lib.muon_workspace_bytes(3, 12, 768) == 256 + _align(3 * 12 * 768 * 4)
-    # tensor-core path: X0, X1 (m x ldx bf16), A, B (m x lda bf16), norm partials
+    # tensor-core path: one completion counter per matrix (u32, after the status
+    # block), then X0, X1 (m x ldx bf16), A, B (m x lda bf16), norm partials
     b, r, c = 2, 300, 130          # tall: m = 130, n = 300
     m, n, ldx, lda = 130, 300, 304, 136
     parts = 4                      # ceil(15 prologue tiles / 4)
-    expect = 256 + 2 * _align(b * m * ldx * 2) + 2 * _align(b * m * lda * 2) + _align(b * parts * 4)
-    assert lib.muon_workspace_bytes(b, r, c) == expect
-    # the grouped size is the sum of the per-group regions
+    buffers = 2 * _align(b * m * ldx * 2) + 2 * _align(b * m * lda * 2) + _align(b * parts * 4)
+    assert lib.muon_workspace_bytes(b, r, c) == 256 + _align(b * 4) + buffers
+    # the grouped size is the sum of the per-group regions (counters only for
+    # tensor-core matrices)
     grp = muon.grouped_workspace_bytes([(3, 12, 768), (2, 300, 130)])
-    assert grp == 256 + _align(3 * 12 * 768 * 4) + (expect - 256)
+    assert grp == 256 + _align(2 * 4) + _align(3 * 12 * 768 * 4) + buffers
+    grp = muon.grouped_workspace_bytes([(70, 64, 64), (2, 300, 130)])
+    assert grp == 256 + _align(72 * 4) + (
+        2 * _align(70 * 64 * 64 * 2) + 2 * _align(70 * 64 * 64 * 2) + _align(70 * 1 * 4)) + buffers
 
 
 def test_trace_without_launches(lib):

@@ -59,7 +59,8 @@ def _rand(shape, std, dtype, seed):
 @pytest.mark.parametrize("shape,gdt", [((2, 256, 384), torch.bfloat16),
                                        ((1, 300, 520), torch.float32),
                                        ((2, 520, 300), torch.bfloat16)])
-def test_prologue_writes_u_then_gram_and_poly(shape, gdt):
+@pytest.mark.parametrize("rounds", [False, True], ids=["per-stage", "persistent"])
+def test_prologue_writes_u_then_gram_and_poly(shape, gdt, rounds):
     """steps=1 leaves X0 = bf16(u or u^T), A = s^2 X0 X0^T and B' = aI + bA + cA^2 in the workspace.
 
     (The polynomial stage folds the a X term of the update into its output, so
@@ -74,14 +75,16 @@ def test_prologue_writes_u_then_gram_and_poly(shape, gdt):
     need = muon.workspace_bytes(b, r, c)
     ws = muon.Workspace(need)
     pg, gg, mg = p.to(DEV), g.to(DEV), m0.to(DEV)
-    with muon.fused_ns(False):      # the staged path keeps X0, A and B' in the workspace
+    # the staged path keeps X0, A and B' in the workspace
+    with muon.fused_ns(False), muon.persistent_rounds(rounds):
         muon.step(pg, gg, mg, momentum=0.9, lr=0.02, weight_decay=0.01, steps=1, workspace=ws)
     torch.cuda.synchronize()
     assert muon.workspace_status(ws) == 0
     raw = ws.tensor
     x0_bytes = b * m * ldx * 2
-    a_off = 256 + 2 * ((x0_bytes + 255) // 256 * 256)
-    X0 = raw[256:256 + x0_bytes].view(torch.bfloat16).view(b, m, ldx)[:, :, :n]
+    x0_off = 256 + (b * 4 + 255) // 256 * 256      # after the status block and the counters
+    a_off = x0_off + 2 * ((x0_bytes + 255) // 256 * 256)
+    X0 = raw[x0_off:x0_off + x0_bytes].view(torch.bfloat16).view(b, m, ldx)[:, :, :n]
     A = raw[a_off:a_off + b * m * lda * 2].view(torch.bfloat16).view(b, m, lda)[:, :, :m]
     a_bytes = (b * m * lda * 2 + 255) // 256 * 256
     Bm = raw[a_off + a_bytes:a_off + a_bytes + b * m * lda * 2].view(torch.bfloat16).view(b, m, lda)[:, :, :m]
@@ -123,8 +126,10 @@ def _fused_shape(r, c):
 
 @pytest.mark.parametrize("shape", NS_SHAPES, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("gdt", [torch.bfloat16, torch.float32])
-def test_ns5_matches_oracle(shape, gdt):
-    _check_ns5(shape, gdt)
+@pytest.mark.parametrize("rounds", [False, True], ids=["per-stage", "persistent"])
+def test_ns5_matches_oracle(shape, gdt, rounds):
+    with muon.persistent_rounds(rounds):
+        _check_ns5(shape, gdt)
 
 
 @pytest.mark.parametrize("shape", FUSED_SHAPES, ids=lambda s: "x".join(map(str, s)))
@@ -133,7 +138,7 @@ def test_ns5_matches_oracle(shape, gdt):
 def test_ns5_fused_range_on_both_paths(shape, gdt, fused):
     assert _fused_shape(*shape[1:])
     n0 = muon.kernel_launch_count()
-    with muon.fused_ns(fused):
+    with muon.fused_ns(fused), muon.persistent_rounds(False):
         _check_ns5(shape, gdt)
     # fused: prologue, the fused rounds, apply; staged: prologue, 3 x 5 stages, apply
     assert muon.kernel_launch_count() - n0 == (3 if fused else 17)
@@ -153,10 +158,10 @@ def _check_ns5(shape, gdt):
 
 
 @pytest.mark.parametrize("steps", [1, 2, 3, 7])
-@pytest.mark.parametrize("fused", [True, False], ids=["fused", "staged"])
-def test_ns5_other_round_counts(steps, fused):
+@pytest.mark.parametrize("path", ["fused", "staged", "persistent"])
+def test_ns5_other_round_counts(steps, path):
     G = _rand((2, 192, 320), 1.0, torch.bfloat16, 11)
-    with muon.fused_ns(fused):
+    with muon.fused_ns(path == "fused"), muon.persistent_rounds(path == "persistent"):
         out = muon.ns5(G.to(DEV), steps=steps)
     torch.cuda.synchronize()
     for i in range(2):
@@ -240,11 +245,13 @@ def _run_workload_and_check(wl, groups_dev, sample=None):
 
 
 @pytest.mark.parametrize("name", ["cfg1", "cfg2", "cfg3"])
-def test_step_matches_oracle_on_small_workloads(name):
+@pytest.mark.parametrize("rounds", [False, True], ids=["per-stage", "persistent"])
+def test_step_matches_oracle_on_small_workloads(name, rounds):
     wl = workloads.get(name)
     cpu = workloads.make_workload(wl, "cpu")       # CPU draws, copied byte for byte
     dev = [(grp, P.to(DEV), G.to(DEV), B.to(DEV)) for grp, P, G, B in cpu]
-    worst = _run_workload_and_check(wl, dev)
+    with muon.persistent_rounds(rounds):
+        worst = _run_workload_and_check(wl, dev)
     print(name, {k: f"{v:.2e}" for k, v in worst.items()})
 
 
@@ -307,8 +314,9 @@ def test_step_options(nesterov, lr_scale, fused, s):
         assert rel(upd, upd_ref) < NS_TOL
 
 
-@pytest.mark.parametrize("fused", [True, False], ids=["fused", "staged"])
-def test_more_groups_than_one_launch_holds(fused):
+@pytest.mark.parametrize("fused,rounds", [(True, False), (False, False), (False, True)],
+                         ids=["fused", "staged", "persistent"])
+def test_more_groups_than_one_launch_holds(fused, rounds):
     # 11 tensor-core groups of different shapes (staged: several grouped launches per
     # stage) plus, for the fused path, 6 more: 17 groups need two fused launches
     shapes = [(1, 64 + 16 * k, 128 + 24 * k) for k in range(11)]
@@ -321,11 +329,13 @@ def test_more_groups_than_one_launch_holds(fused):
         ref.append((P, G, B0))
         groups.append((P.to(DEV), G.to(DEV), B0.to(DEV)))
     n0 = muon.kernel_launch_count()
-    with muon.fused_ns(fused):
+    with muon.fused_ns(fused), muon.persistent_rounds(rounds):
         muon.step_grouped(groups, momentum=0.95, lr=0.02, weight_decay=0.01)
     torch.cuda.synchronize()
     if fused:   # 17 groups: two launches each of prologue, fused rounds and apply
         assert muon.kernel_launch_count() - n0 == 6
+    if rounds:  # 11 groups: prologue, two persistent launches (8 + 3 groups), apply
+        assert muon.kernel_launch_count() - n0 == 4
     for (P, G, B0), (pd, _, _) in zip(ref, groups):
         for i in range(P.shape[0]):
             p_ref, _, _ = oracle.muon_step(f64(P[i]), f64(G[i]), f64(B0[i]), momentum=0.95,
@@ -334,8 +344,14 @@ def test_more_groups_than_one_launch_holds(fused):
             assert rel(upd, upd_ref) < NS_TOL
 
 
-def test_deterministic_and_checkpoint_resume():
+@pytest.mark.parametrize("rounds", [False, True], ids=["per-stage", "persistent"])
+def test_deterministic_and_checkpoint_resume(rounds):
     """Two runs give identical bits; step -> save -> load -> step equals two straight steps."""
+    with muon.persistent_rounds(rounds):
+        _deterministic_and_checkpoint_resume()
+
+
+def _deterministic_and_checkpoint_resume():
     wl = workloads.get("cfg2")
     cpu = workloads.make_workload(wl, "cpu")
 
@@ -367,7 +383,7 @@ def test_launch_count_and_trace():
     assert all(r["ms"] > 0 for r in recs)
     n0 = muon.kernel_launch_count()
     muon.trace_begin(64)
-    with muon.fused_ns(False):
+    with muon.fused_ns(False), muon.persistent_rounds(False):
         muon.ns5(G)
     recs = muon.trace_end()
     assert muon.kernel_launch_count() - n0 == 1 + 3 * 5 + 1
@@ -375,6 +391,28 @@ def test_launch_count_and_trace():
     assert kinds[0] == "prologue" and kinds[-1] == "apply"
     assert kinds[1:16] == ["gram", "poly", "update"] * 5
     assert all(r["ms"] > 0 for r in recs)
+
+
+def test_automatic_rounds_mode():
+    # short rounds (a few hundred tiles) take the persistent launch by default
+    G = _rand((2, 300, 520), 1.0, torch.bfloat16, 5).to(DEV)
+    muon.trace_begin(64)
+    with muon.persistent_rounds("auto"):
+        muon.ns5(G)
+    assert [r["kind"] for r in muon.trace_end()] == ["prologue", "rounds", "apply"]
+    assert muon.set_persistent_rounds("auto") == 2     # the default
+
+
+def test_persistent_launch_count_and_trace():
+    G = _rand((2, 300, 520), 1.0, torch.bfloat16, 5).to(DEV)
+    n0 = muon.kernel_launch_count()
+    muon.trace_begin(64)
+    with muon.persistent_rounds(True):
+        muon.ns5(G)
+    recs = muon.trace_end()
+    assert muon.kernel_launch_count() - n0 == 3
+    assert [r["kind"] for r in recs] == ["prologue", "rounds", "apply"]
+    assert recs[1]["flops"] > 0 and all(r["ms"] > 0 for r in recs)
 
 
 def test_mixed_call_runs_every_matrix_staged():
@@ -387,7 +425,8 @@ def test_mixed_call_runs_every_matrix_staged():
         groups.append((P.to(DEV), G.to(DEV), torch.zeros(s, device=DEV)))
     n0 = muon.kernel_launch_count()
     muon.trace_begin(64)
-    muon.step_grouped(groups, momentum=0.95, lr=0.02, weight_decay=0.01)
+    with muon.persistent_rounds(False):
+        muon.step_grouped(groups, momentum=0.95, lr=0.02, weight_decay=0.01)
     kinds = [r["kind"] for r in muon.trace_end()]
     assert muon.kernel_launch_count() - n0 == 17 and "fused_ns" not in kinds
     for (P, G), (pd, _, _) in zip(ref, groups):
