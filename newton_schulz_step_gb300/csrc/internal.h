@@ -54,7 +54,7 @@ struct PrologueLaunch {
   int n_groups;
   int total_blocks;
   float beta;
-  int wait_prior;         // 1: wait for the preceding grid (PDL) before exiting
+  int wait_prior;         // 1: block 0 waits for the preceding grid (PDL) before exiting
   unsigned int* zero;     // counters the launch zeroes (block 0), or null
   int n_zero;
 };

@@ -17,7 +17,7 @@
 // thread moves 2 x 8 consecutive elements of a tile row with 16-byte accesses;
 // rows > cols tiles are transposed through shared memory so the X stores stay
 // coalesced.  Launched as a programmatic dependent of the small-matrix kernel,
-// it overlaps that kernel and waits for it only before exiting.
+// it overlaps that kernel; one of its blocks waits for it before exiting.
 #include "internal.h"
 
 namespace muon {
@@ -201,8 +201,11 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
     for (int w = 0; w < 8; ++w) t += red[w];
     A.parts[static_cast<size_t>(mat) * A.nparts + part] = t;
   }
-  // Programmatic dependent of the small-matrix kernel: finish only after it.
-  if (L.wait_prior) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Programmatic dependent of the small-matrix kernel: the grid finishes only
+  // after it.  One block waiting is enough for that (the grid completes when its
+  // last block exits); if every block waited, the first wave would hold its SMs
+  // until the small kernel ended and the rest of the prologue could not start.
+  if (L.wait_prior && blockIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ apply
