@@ -451,6 +451,7 @@ KERNEL_SOURCES = {
     "gram": ("ns_gemm.cu", "ptx.cuh"), "poly": ("ns_gemm.cu", "ptx.cuh"),
     "update": ("ns_gemm.cu", "ptx.cuh"), "prologue": ("prologue.cu",), "apply": ("prologue.cu",),
     "small_ns": ("ns_small.cu",), "fused_ns": ("ns_fused.cu", "ptx.cuh"), "adam": ("adam.cu",),
+    "rounds": ("ns_gemm.cu", "ptx.cuh"),
 }
 
 
