@@ -331,28 +331,47 @@ def run_gpu(args, wl):
     h2d = sum(t.numel() * t.element_size() for t in host_g)
     d2h = sum(t.numel() * t.element_size() for t in host_p)
     e2e_steps = max(1, min(args.steps, 20))
-    # Step k's gradient upload runs on a copy stream as soon as step k-1 has
-    # finished (its prologue has read the previous gradients), beside step
-    # k-1's parameter read-back; step k waits for its upload and, in stream
-    # order, for that read-back (it writes the parameters).
-    copy_stream = torch.cuda.Stream(device=dev)
+    # Three streams and two device gradient buffers.  Step k's gradient upload
+    # (copy stream in) goes into buffer k % 2 once step k-2 is done with it, so it
+    # runs beside step k-1; step k runs on the main stream once its upload is in;
+    # its parameters are then snapshotted on the device (once the snapshot of
+    # step k-1 has been read back) and read back to the host from the snapshot
+    # (copy stream out) while step k+1 computes.  Every copy of every step is
+    # inside the timed region.
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    grads2 = [G.clone() for _, G, _ in tensors]
+    step2 = muon.GroupedStep([(P, G2, B) for (P, _, B), G2 in zip(tensors, grads2)],
+                             momentum=wl.momentum, lr=wl.lr, weight_decay=wl.weight_decay,
+                             nesterov=wl.nesterov, steps=wl.steps)
+    dev_g = [[G for _, G, _ in tensors], grads2]
+    steps_ab = [step, step2]
+    snap = [torch.empty_like(P) for P, _, _ in tensors]
     ev_in = [torch.cuda.Event() for _ in range(e2e_steps)]
     ev_done = [torch.cuda.Event() for _ in range(e2e_steps)]
+    ev_out = [torch.cuda.Event() for _ in range(e2e_steps)]
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
     e0.record(stream)
     for k in range(e2e_steps):
-        copy_stream.wait_event(ev_done[k - 1] if k > 0 else e0)
-        with torch.cuda.stream(copy_stream):
-            for (_, G, _), hg in zip(tensors, host_g):
+        up.wait_event(ev_done[k - 2] if k > 1 else e0)
+        with torch.cuda.stream(up):
+            for G, hg in zip(dev_g[k % 2], host_g):
                 G.copy_(hg, non_blocking=True)
-            ev_in[k].record(copy_stream)
+            ev_in[k].record(up)
         stream.wait_event(ev_in[k])
-        step()
+        steps_ab[k % 2]()
+        if k > 0:
+            stream.wait_event(ev_out[k - 1])
+        for (P, _, _), sp in zip(tensors, snap):
+            sp.copy_(P, non_blocking=True)
         ev_done[k].record(stream)
-        for (P, _, _), hp in zip(tensors, host_p):
-            hp.copy_(P, non_blocking=True)
+        down.wait_event(ev_done[k])
+        with torch.cuda.stream(down):
+            for sp, hp in zip(snap, host_p):
+                hp.copy_(sp, non_blocking=True)
+            ev_out[k].record(down)
+    stream.wait_event(ev_out[e2e_steps - 1])
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -361,8 +380,10 @@ def run_gpu(args, wl):
     e2e = {"value": e2e_units / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "ms_per_step": e2e_ms / e2e_steps,
-           "schedule": "gradient upload of step k on a copy stream beside the parameter "
-                       "read-back of step k-1; every copy inside the timed region"}
+           "schedule": "gradient upload (copy stream, two device gradient buffers) and "
+                       "parameter read-back from a device snapshot (second copy stream) of "
+                       "neighbouring steps overlap the compute; every copy of every step "
+                       "inside the timed region"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
