@@ -233,6 +233,11 @@ int muon_set_fused_ns(int enable);
  * mode = 2 (the default): 1 for groups whose rounds are short (estimated
  * tensor-core time of a round under 400 us), where the stage boundaries weigh
  * most; 0 otherwise.  Same results and workspace size in every mode.
+ * The persistent launch needs all of its clusters (one per two SMs that fit
+ * at once) resident together, since tiles wait for tiles of other clusters:
+ * kernels on other streams that hold SMs delay it, and if they hold them for
+ * more than its 2 s wait limit the step reports MUON_ERR_TIMEOUT.  Mode 0 has
+ * no such requirement.
  * Process-wide; affects calls made afterwards.  Returns the previous mode, or
  * -1 (nothing changed) if mode is not 0, 1 or 2.
  */
