@@ -120,8 +120,8 @@ struct GemmLaunch {
   CUtensorMap tm_b[kMaxProblems];   // operand B half tiles (box 64 x 128, or 64 x 64 for X)
   CUtensorMap tm_at[kMaxProblems];  // symmetric operand A read transposed (box 64 x 64)
   CUtensorMap tm_bt[kMaxProblems];  // Poly: symmetric operand B read transposed (box 64 x 64)
-  CUtensorMap tm_out[kMaxProblems]; // output blocks (box 32 x 32 bf16, 64-byte swizzle)
-  CUtensorMap tm_in[kMaxProblems];  // Poly: blocks of A for the b A term (box 32 x 32, 64-byte swizzle)
+  CUtensorMap tm_out[kMaxProblems]; // output blocks (box 64 x 32 bf16, 128-byte swizzle)
+  CUtensorMap tm_in[kMaxProblems];  // Poly: blocks of A for the b A term (box 64 x 32, 128-byte swizzle)
   GemmProblem prob[kMaxProblems];
   int n_prob;
   int total_tiles;                  // pair tiles
@@ -151,13 +151,13 @@ struct RoundsProblem {
 struct RoundsLaunch {
   CUtensorMap x_op[kMaxProblems][2];   // X buffer 0/1 as K-major operand (box 64 x 128)
   CUtensorMap x_mn[kMaxProblems][2];   // X buffer 0/1 as MN-major operand (box 64 x 64)
-  CUtensorMap x_out[kMaxProblems][2];  // X buffer 0/1 output blocks (32 x 32, 64-byte swizzle)
+  CUtensorMap x_out[kMaxProblems][2];  // X buffer 0/1 output blocks (64 x 32, 128-byte swizzle)
   CUtensorMap a_op[kMaxProblems];      // A (box 64 x 128)
   CUtensorMap a_mn[kMaxProblems];      // A read transposed (box 64 x 64)
-  CUtensorMap a_blk[kMaxProblems];     // A 32 x 32 blocks (Gram output, Poly b A input)
+  CUtensorMap a_blk[kMaxProblems];     // A 64 x 32 blocks (Gram output, Poly b A input)
   CUtensorMap b_op[kMaxProblems];      // B' (box 64 x 128)
   CUtensorMap b_mn[kMaxProblems];      // B' read transposed (box 64 x 64)
-  CUtensorMap b_out[kMaxProblems];     // B' 32 x 32 output blocks
+  CUtensorMap b_out[kMaxProblems];     // B' 64 x 32 output blocks
   RoundsProblem prob[kMaxProblems];
   int n_prob;
   int steps;

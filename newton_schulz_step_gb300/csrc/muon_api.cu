@@ -154,11 +154,9 @@ bool operand_tmap(CUtensorMap* tm, const void* base, int cols, int rows, int bat
   return make_tmap(tm, base, cols, rows, batch, ld, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// Epilogue output blocks of 32 x 32: 64-byte swizzle (direct) or none (mirror).
-bool output_tmap(CUtensorMap* tm, const void* base, int cols, int rows, int batch, int ld,
-                 bool swizzled) {
-  return make_tmap(tm, base, cols, rows, batch, ld, 32, 32,
-                   swizzled ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE);
+// Epilogue blocks of 32 rows x 64 columns (128 bytes), 128-byte swizzle.
+bool output_tmap(CUtensorMap* tm, const void* base, int cols, int rows, int batch, int ld) {
+  return make_tmap(tm, base, cols, rows, batch, ld, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // ------------------------------------------------------------ planning
@@ -345,19 +343,19 @@ muon_status build_gemm(GemmLaunch& L, const std::vector<GPlan*>& chunk, int stag
     if (stage == kStageGram) {          // A = s^2 X X^T
       ok = operand_tmap(&L.tm_a[i], xc, g.n, g.m, g.batch, g.ldx, kTileM) &&
            operand_tmap(&L.tm_b[i], xc, g.n, g.m, g.batch, g.ldx, kTileM) &&
-           output_tmap(&L.tm_out[i], ws + g.am, g.m, g.m, g.batch, g.lda, true);
+           output_tmap(&L.tm_out[i], ws + g.am, g.m, g.m, g.batch, g.lda);
     } else if (stage == kStagePoly) {   // B' = a I + b A + c A A
       ok = operand_tmap(&L.tm_a[i], ws + g.am, g.m, g.m, g.batch, g.lda, kTileM) &&
            operand_tmap(&L.tm_b[i], ws + g.am, g.m, g.m, g.batch, g.lda, kTileM) &&
            operand_tmap(&L.tm_at[i], ws + g.am, g.m, g.m, g.batch, g.lda, 64) &&
            operand_tmap(&L.tm_bt[i], ws + g.am, g.m, g.m, g.batch, g.lda, 64) &&
-           output_tmap(&L.tm_out[i], ws + g.bm, g.m, g.m, g.batch, g.lda, true) &&
-           output_tmap(&L.tm_in[i], ws + g.am, g.m, g.m, g.batch, g.lda, true);
+           output_tmap(&L.tm_out[i], ws + g.bm, g.m, g.m, g.batch, g.lda) &&
+           output_tmap(&L.tm_in[i], ws + g.am, g.m, g.m, g.batch, g.lda);
     } else {                            // X' = s B' X
       ok = operand_tmap(&L.tm_a[i], ws + g.bm, g.m, g.m, g.batch, g.lda, kTileM) &&
            operand_tmap(&L.tm_at[i], ws + g.bm, g.m, g.m, g.batch, g.lda, 64) &&
            operand_tmap(&L.tm_b[i], xc, g.n, g.m, g.batch, g.ldx, 64) &&
-           output_tmap(&L.tm_out[i], xn, g.n, g.m, g.batch, g.ldx, true);
+           output_tmap(&L.tm_out[i], xn, g.n, g.m, g.batch, g.ldx);
     }
     if (!ok) return MUON_ERR_CUDA;
   }
@@ -417,14 +415,14 @@ muon_status build_rounds(RoundsLaunch& R, const std::vector<GPlan*>& chunk, cons
       uint8_t* xb = ws + (b ? g.x1 : g.x0);
       ok = ok && operand_tmap(&R.x_op[i][b], xb, g.n, g.m, g.batch, g.ldx, kTileM) &&
            operand_tmap(&R.x_mn[i][b], xb, g.n, g.m, g.batch, g.ldx, 64) &&
-           output_tmap(&R.x_out[i][b], xb, g.n, g.m, g.batch, g.ldx, true);
+           output_tmap(&R.x_out[i][b], xb, g.n, g.m, g.batch, g.ldx);
     }
     ok = ok && operand_tmap(&R.a_op[i], ws + g.am, g.m, g.m, g.batch, g.lda, kTileM) &&
          operand_tmap(&R.a_mn[i], ws + g.am, g.m, g.m, g.batch, g.lda, 64) &&
-         output_tmap(&R.a_blk[i], ws + g.am, g.m, g.m, g.batch, g.lda, true) &&
+         output_tmap(&R.a_blk[i], ws + g.am, g.m, g.m, g.batch, g.lda) &&
          operand_tmap(&R.b_op[i], ws + g.bm, g.m, g.m, g.batch, g.lda, kTileM) &&
          operand_tmap(&R.b_mn[i], ws + g.bm, g.m, g.m, g.batch, g.lda, 64) &&
-         output_tmap(&R.b_out[i], ws + g.bm, g.m, g.m, g.batch, g.lda, true);
+         output_tmap(&R.b_out[i], ws + g.bm, g.m, g.m, g.batch, g.lda);
     if (!ok) return MUON_ERR_CUDA;
   }
   R.n_prob = static_cast<int>(order.size());

@@ -27,7 +27,7 @@
 // 192 threads:
 //   warp 0      TMA producer (one lane) into a ring of swizzled smem stages
 //   warp 1      TMEM allocator; in the even CTA also the tcgen05.mma issuer
-//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator, fp32 math, 32 x 32
+//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator, fp32 math, 32 x 64
 //               blocks staged in shared memory and written by TMA bulk stores
 // The pair computes a 256 x 256 tile with cta_group::2 MMAs (M = 256): CTA r
 // holds tile rows 2p + r (128 rows of A) and the r-th 128-column half of B in
@@ -67,8 +67,8 @@ struct Cfg {
   static constexpr int kTmemCols = 2 * kBN;              // two 128 x 256 fp32 accumulators
   static constexpr int kEpiWarps = 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
-  static constexpr int kSlots = 3;                       // per epilogue warp
-  static constexpr int kSlotBytes = 2048;                // one 32 x 32 bf16 block
+  static constexpr int kSlots = 2;                       // per epilogue warp
+  static constexpr int kSlotBytes = 4096;                // one 32 x 64 bf16 block
   static constexpr int kStagingBytes = kEpiWarps * kSlots * kSlotBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmem = kStages * kStageBytes + kStagingBytes + kBarBytes + 1024;
@@ -82,8 +82,8 @@ struct TileCtx {
   const CUtensorMap* at;   // operand A read transposed (symmetric A), boxes of 64 x 64
   const CUtensorMap* b;    // operand B: K-major 64 x 128 (Gram, Poly) or 64 x 64 (Update, X)
   const CUtensorMap* bt;   // Poly: operand B read transposed, 64 x 64
-  const CUtensorMap* out;  // output 32 x 32 blocks
-  const CUtensorMap* in;   // Poly: A 32 x 32 blocks (the b A term)
+  const CUtensorMap* out;  // output 32 x 64 blocks
+  const CUtensorMap* in;   // Poly: A 32 x 64 blocks (the b A term)
   int mat, pr, tn;         // matrix, pair row (pr >= tiles_m: no rows), tile column
   int m, n, k_blocks;
   const float* parts;      // first round: norm partials of the batch
@@ -265,33 +265,36 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&b2);
 }
 
-// Output staging.  Each epilogue warp owns kSlots 2 KB slots used in turn,
-// each holding the warp's 32 x 32 block of the output, bf16, 64-byte rows with
-// the 64-byte swizzle TMA expects (16-byte unit u of row r sits at unit
-// u ^ ((r >> 1) & 3)), written with 16-byte stores and stored to global memory
-// by one TMA bulk store.  Poly first loads its A block into the slot by TMA.
-__device__ __forceinline__ uint32_t sw64(int r, int c) {
-  return static_cast<uint32_t>(r * 64 + ((((c >> 3) ^ (r >> 1)) & 3) << 4) + (c & 7) * 2);
+// Output staging.  Each epilogue warp owns kSlots 4 KB slots used in turn,
+// each holding the warp's 32 x 64 block of the output, bf16, 128-byte rows
+// with the 128-byte swizzle TMA expects (16-byte unit u of row r sits at unit
+// u ^ (r & 7)), written with 16-byte stores and stored to global memory by one
+// TMA bulk store.  Poly first loads its A block into the slot by TMA.  (Blocks
+// of 32 x 64 rather than 32 x 32 halve the bulk copies a tile issues.)
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + ((((c >> 3) ^ r) & 7) << 4) + (c & 7) * 2);
 }
 
-__device__ __forceinline__ void stage_row_sw64(uint8_t* blk, int r, const float (&v)[32]) {
+// Columns 32 h .. 32 h + 31 of row r.
+__device__ __forceinline__ void stage_half_sw128(uint8_t* blk, int r, int h,
+                                                 const float (&v)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const uint4 w = make_uint4(pack_bf2(v[8 * q + 0], v[8 * q + 1]),
                                pack_bf2(v[8 * q + 2], v[8 * q + 3]),
                                pack_bf2(v[8 * q + 4], v[8 * q + 5]),
                                pack_bf2(v[8 * q + 6], v[8 * q + 7]));
-    *reinterpret_cast<uint4*>(blk + sw64(r, 8 * q)) = w;
+    *reinterpret_cast<uint4*>(blk + sw128(r, 32 * h + 8 * q)) = w;
   }
 }
 
 // ------------------------------------------------------------ epilogue warps
 // Warp w (2..5) owns TMEM lanes 32*(w&3).. (32 rows of the 128-row tile) and
-// walks the tile's 256 columns in 8 chunks of 32.
+// walks the tile's 256 columns in 4 units of 64 (two 32-column TMEM loads each).
 struct EpiState {
   int acc = 0;
   uint32_t acc_phase = 0;
-  int slot = 0;         // next staging slot (ring of kSlots)
+  int slot = 0;         // next staging slot (alternating)
   uint32_t in_par = 0;  // Poly: parity of each slot's next input load
 };
 
@@ -305,7 +308,8 @@ __device__ bool epilogue_tile(const TileCtx& T, const GemmScalars& k, uint64_t* 
                               int quarter, int lane, int rank, const unsigned int* dep,
                               unsigned int dep_target) {
   using C = Cfg;
-  constexpr int kChunks = C::kBN / 32;
+  static_assert(C::kSlots == 2, "the staging slots alternate");
+  constexpr int kUnits = C::kBN / 64;
   constexpr bool kSym = STAGE <= kStagePoly;
   constexpr bool kPoly = STAGE == kStagePoly;
   __syncwarp();
@@ -316,23 +320,25 @@ __device__ bool epilogue_tile(const TileCtx& T, const GemmScalars& k, uint64_t* 
   const int i0 = tm * kTileM + quarter * 32;  // first row of this warp
   const int ncols = kSym ? T.m : T.n;
   const int jt = T.tn * C::kBN;
-  // live chunks: c_lo <= ch < c_hi (rows in range, columns in range)
-  const int c_lo = 0;
-  const int c_hi = i0 < T.m ? min(kChunks, (ncols - jt + 31) / 32) : 0;
-  // Poly: the first two live chunks' A blocks into their slots
+  // live units: rows in range, columns in range
+  const int u_hi = i0 < T.m ? min(kUnits, (ncols - jt + 63) / 64) : 0;
+  // Poly: the first two live units' A blocks into the two slots
   if constexpr (kPoly) {
     int ok = 1;
-    if (lane == 0) {
-      if (dep != nullptr && c_hi > c_lo) {
+    if (lane == 0 && u_hi > 0) {
+      if (dep != nullptr) {
         if (!ptx::wait_counter(dep, dep_target, abort_flag)) ok = 0;
         ptx::fence_proxy_async_global();
       }
-      for (int q = 0; ok && q < 2 && c_lo + q < c_hi; ++q) {
-        const int sl = (es.slot + q) % C::kSlots;
-        if (q == 0) ptx::bulk_wait_read<2>(); else ptx::bulk_wait_read<1>();
-        ptx::mbar_arrive_expect_tx(&my_in[sl], 2048);
-        ptx::tma_load_3d(my_slots + sl * C::kSlotBytes, T.in, jt + 32 * (c_lo + q), i0, T.mat,
-                         &my_in[sl]);
+      if (ok) {
+        // both slots' earlier stores have read their data
+        ptx::bulk_wait_read<0>();
+        for (int q = 0; q < 2 && q < u_hi; ++q) {
+          const int sl = es.slot ^ q;
+          ptx::mbar_arrive_expect_tx(&my_in[sl], C::kSlotBytes);
+          ptx::tma_load_3d(my_slots + sl * C::kSlotBytes, T.in, jt + 64 * q, i0, T.mat,
+                           &my_in[sl]);
+        }
       }
     }
     if (__shfl_sync(0xffffffffu, ok, 0) == 0) return false;
@@ -346,67 +352,68 @@ __device__ bool epilogue_tile(const TileCtx& T, const GemmScalars& k, uint64_t* 
                          static_cast<uint32_t>(es.acc * C::kBN);
   bool failed = false;
 #pragma unroll 1
-  for (int ch = c_lo; ch < c_hi; ++ch) {
-    const int j0 = jt + ch * 32;
+  for (int u = 0; u < u_hi; ++u) {
+    const int j0 = jt + u * 64;
     uint8_t* blk = my_slots + es.slot * C::kSlotBytes;
-    uint32_t ev[16];
     if constexpr (kPoly) {
       const uint32_t par = (es.in_par >> es.slot) & 1u;
       if (!ptx::mbar_wait(&my_in[es.slot], par, abort_flag)) failed = true;
       es.in_par ^= 1u << es.slot;
-      __syncwarp();
-      // row `lane` of the A block, 64-byte swizzled like the output blocks
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 w = *reinterpret_cast<const uint4*>(blk + sw64(lane, 8 * q));
-        ev[4 * q + 0] = w.x;
-        ev[4 * q + 1] = w.y;
-        ev[4 * q + 2] = w.z;
-        ev[4 * q + 3] = w.w;
-      }
     } else {
-      // the slot's previous bulk store (kSlots - 1 chunks ago) has read its data
+      // the slot's previous bulk store (two units ago) has read its data
       if (lane == 0) ptx::bulk_wait_read<C::kSlots - 1>();
     }
     __syncwarp();
-    uint32_t v[32];
-    ptx::tmem_ld32(tbase + static_cast<uint32_t>(ch * 32), v);
-    ptx::tmem_ld_wait();
-    float val[32];
-    if constexpr (STAGE == kStageGram) {
 #pragma unroll
-      for (int q = 0; q < 32; ++q) val[q] = __uint_as_float(v[q]) * (s * s);
-    } else if constexpr (kPoly) {
+    for (int h = 0; h < 2; ++h) {
+      uint32_t v[32];
+      ptx::tmem_ld32_sync(tbase + static_cast<uint32_t>(u * 64 + h * 32), v);
+      float val[32];
+      if constexpr (STAGE == kStageGram) {
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        val[2 * q] = fmaf(k.c, __uint_as_float(v[2 * q]), k.b * bf_lo(ev[q]));
-        val[2 * q + 1] = fmaf(k.c, __uint_as_float(v[2 * q + 1]), k.b * bf_hi(ev[q]));
+        for (int q = 0; q < 32; ++q) val[q] = __uint_as_float(v[q]) * (s * s);
+      } else if constexpr (kPoly) {
+        // row `lane`, columns 32 h.. of the A block (each lane reads and then
+        // overwrites only its own row)
+        uint32_t ev[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 w = *reinterpret_cast<const uint4*>(blk + sw128(lane, 32 * h + 8 * q));
+          ev[4 * q + 0] = w.x;
+          ev[4 * q + 1] = w.y;
+          ev[4 * q + 2] = w.z;
+          ev[4 * q + 3] = w.w;
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          val[2 * q] = fmaf(k.c, __uint_as_float(v[2 * q]), k.b * bf_lo(ev[q]));
+          val[2 * q + 1] = fmaf(k.c, __uint_as_float(v[2 * q + 1]), k.b * bf_hi(ev[q]));
+        }
+        // B' = a I + b A + c A A: the update then needs no a X term
+        if (j0 + 32 * h == i0) {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) val[q] += (q == lane) ? k.a : 0.f;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 32; ++q) val[q] = s * __uint_as_float(v[q]);
       }
-      // B' = a I + b A + c A A: the update then needs no a X term
-      if (j0 == i0) {
-#pragma unroll
-        for (int q = 0; q < 32; ++q) val[q] += (q == lane) ? k.a : 0.f;
-      }
-    } else {
-#pragma unroll
-      for (int q = 0; q < 32; ++q) val[q] = s * __uint_as_float(v[q]);
+      stage_half_sw128(blk, lane, h, val);
     }
-    stage_row_sw64(blk, lane, val);
     ptx::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
       ptx::tma_store_3d(T.out, j0, i0, T.mat, blk);
       ptx::bulk_commit();
-      // Poly: the A block two live chunks ahead goes into the slot whose
-      // store was issued one chunk ago
-      if (kPoly && ch + 2 < c_hi) {
-        const int sl = (es.slot + 2) % C::kSlots;
-        ptx::bulk_wait_read<1>();
-        ptx::mbar_arrive_expect_tx(&my_in[sl], 2048);
-        ptx::tma_load_3d(my_slots + sl * C::kSlotBytes, T.in, j0 + 64, i0, T.mat, &my_in[sl]);
+      // Poly: the A block two units ahead goes into this slot once the store
+      // just issued has read it
+      if (kPoly && u + 2 < u_hi) {
+        ptx::bulk_wait_read<0>();
+        ptx::mbar_arrive_expect_tx(&my_in[es.slot], C::kSlotBytes);
+        ptx::tma_load_3d(blk, T.in, j0 + 128, i0, T.mat, &my_in[es.slot]);
       }
     }
-    es.slot = (es.slot + 1) % C::kSlots;
+    es.slot ^= 1;
   }
   ptx::tc_fence_before();
   __syncwarp();
