@@ -46,12 +46,15 @@
 //                          launch per stage, chained by programmatic
 //                          dependent launch)
 //   ns_rounds_kernel       every stage of every round of a chunk of groups in
-//                          one launch: a tile waits (in the producer) for the
-//                          per-matrix completion counter of the stages before
-//                          it, which the epilogue warps advance once their
-//                          stores of a tile are complete, so one matrix's
-//                          next stage can start while other matrices still
-//                          finish the current one.
+//                          one launch: a tile waits for the per-matrix
+//                          completion counter of the stages before it, which
+//                          the epilogue warps advance once their stores of a
+//                          tile are complete, so one matrix's next stage can
+//                          start while other matrices still finish the current
+//                          one.  A seventh warp (the scheduler) decodes the
+//                          tiles and does these waits, and hands ready tiles to
+//                          the producer through a small queue, so that the
+//                          producer only issues copies.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -67,10 +70,12 @@ struct Cfg {
   static constexpr int kTmemCols = 2 * kBN;              // two 128 x 256 fp32 accumulators
   static constexpr int kEpiWarps = 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kRoundsThreads = kThreads + 32;   // + the scheduler warp
+  static constexpr int kQueue = 8;                        // ready tiles scheduler -> producer
   static constexpr int kSlots = 2;                       // per epilogue warp
   static constexpr int kSlotBytes = 4096;                // one 32 x 64 bf16 block
   static constexpr int kStagingBytes = kEpiWarps * kSlots * kSlotBytes;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
   static constexpr int kSmem = kStages * kStageBytes + kStagingBytes + kBarBytes + 1024;
   // completion-counter increments per stored pair tile: every epilogue warp of both CTAs
   static constexpr unsigned int kSignalsPerTile = 2 * kEpiWarps;
@@ -431,6 +436,7 @@ struct Smem {
   uint8_t* ring;
   uint8_t* staging;
   uint64_t *full, *empty, *acc_full, *acc_empty, *drain, *in_bar;
+  uint64_t *q_full, *q_empty;  // rounds kernel: the ready-tile queue
   uint32_t* tmem_slot;
   volatile int* abort_flag;
 };
@@ -449,7 +455,9 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* smem_raw) {
   m.acc_empty = m.acc_full + 2;
   m.drain = m.acc_empty + 2;
   m.in_bar = m.drain + 1;  // Poly: one per epilogue warp and slot
-  m.tmem_slot = reinterpret_cast<uint32_t*>(m.in_bar + C::kEpiWarps * C::kSlots);
+  m.q_full = m.in_bar + C::kEpiWarps * C::kSlots;
+  m.q_empty = m.q_full + C::kQueue;
+  m.tmem_slot = reinterpret_cast<uint32_t*>(m.q_empty + C::kQueue);
   m.abort_flag = reinterpret_cast<volatile int*>(m.tmem_slot + 1);
   return m;
 }
@@ -468,6 +476,10 @@ __device__ __forceinline__ uint32_t setup_cta(const Smem& m, int warp) {
     }
     ptx::mbar_init(m.drain, 1);
     for (int k = 0; k < C::kEpiWarps * C::kSlots; ++k) ptx::mbar_init(&m.in_bar[k], 1);
+    for (int k = 0; k < C::kQueue; ++k) {
+      ptx::mbar_init(&m.q_full[k], 1);   // the scheduler, entry written
+      ptx::mbar_init(&m.q_empty[k], 1);  // the producer, entry read
+    }
     *m.abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -718,9 +730,12 @@ __device__ __forceinline__ TileCtx rounds_ctx(const RoundsLaunch& L, const Item&
   return T;
 }
 
-__global__ void __launch_bounds__(Cfg::kThreads, 1)
+// Warps: 0 producer, 1 TMEM and MMA issuer, 2..5 epilogue, 6 scheduler.
+__global__ void __launch_bounds__(Cfg::kRoundsThreads, 1)
     ns_rounds_kernel(const __grid_constant__ RoundsLaunch L) {
   extern __shared__ uint8_t smem_raw[];
+  // ready tiles: round | stage << 8 | problem << 12, matrix, pair row, tile column
+  __shared__ int4 queue[Cfg::kQueue];
   const Smem sm = carve_smem(smem_raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -744,18 +759,27 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       }
       ProdState ps;
       const uint32_t leader_full0 = ptx::mapa_shared(ptx::smem_u32(sm.full), 0);
-      for (int i = first_tile(); i < L.total_items; i += tile_stride()) {
-        const Item it = decode_item(L, i);
-        // the operands of this tile are the stored outputs of the stages before
-        const unsigned int target = dep_target(L, it);
-        if (target > 0) {
-          if (!ptx::wait_counter(L.done + L.prob[it.p].done_begin + it.mat, target,
-                                 sm.abort_flag)) {
-            record_failure(L.status, sm.abort_flag, kErrTimeoutDepend);
-            break;
-          }
-          ptx::fence_proxy_async_global();
+      int n = 0;
+      for (int i = first_tile(); i < L.total_items; i += tile_stride(), ++n) {
+        const int q = n % Cfg::kQueue;
+        if (!ptx::mbar_wait(&sm.q_full[q], static_cast<uint32_t>((n / Cfg::kQueue) & 1),
+                            sm.abort_flag)) {
+          record_failure(L.status, sm.abort_flag, kErrTimeoutProducer);
+          break;
         }
+        const int4 e = queue[q];
+        ptx::mbar_arrive(&sm.q_empty[q]);
+        Item it;
+        it.r = e.x & 0xFF;
+        it.s = (e.x >> 8) & 0xF;
+        it.p = e.x >> 12;
+        it.mat = e.y;
+        it.pr = e.z;
+        it.tn = e.w;
+        // the scheduler acquired the counter of the stages before (its queue
+        // barrier passes that on); the operands were stored through the async
+        // proxy and are read through it
+        ptx::fence_proxy_async_global();
         const TileCtx T = rounds_ctx(L, it);
         bool ok;
         if (it.s == kStageGram)
@@ -773,6 +797,29 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
       }
       drain_producer(ps, sm.empty, L.status, sm.abort_flag);
+    }
+  } else if (warp == 2 + Cfg::kEpiWarps) {
+    // scheduler: the tiles in order, each once the stages before it (of its
+    // matrix) are stored, into the queue
+    if (lane == 0) {
+      int n = 0;
+      for (int i = first_tile(); i < L.total_items; i += tile_stride(), ++n) {
+        const int q = n % Cfg::kQueue;
+        if (!ptx::mbar_wait(&sm.q_empty[q], static_cast<uint32_t>(((n / Cfg::kQueue) & 1) ^ 1),
+                            sm.abort_flag)) {
+          record_failure(L.status, sm.abort_flag, kErrTimeoutProducer);
+          break;
+        }
+        const Item it = decode_item(L, i);
+        const unsigned int target = dep_target(L, it);
+        if (target > 0 &&
+            !ptx::wait_counter(L.done + L.prob[it.p].done_begin + it.mat, target, sm.abort_flag)) {
+          record_failure(L.status, sm.abort_flag, kErrTimeoutDepend);
+          break;
+        }
+        queue[q] = make_int4(it.r | (it.s << 8) | (it.p << 12), it.mat, it.pr, it.tn);
+        ptx::mbar_arrive(&sm.q_full[q]);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
@@ -865,7 +912,7 @@ cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_
 // Clusters that fit on the device at once (one CTA per SM), queried once per
 // device and kernel.
 template <typename K>
-static cudaError_t max_clusters(K kernel, int slot, int sms, int* out) {
+static cudaError_t max_clusters(K kernel, int slot, int threads, int sms, int* out) {
   static int cache[4][64] = {{0}};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -880,7 +927,7 @@ static cudaError_t max_clusters(K kernel, int slot, int sms, int* out) {
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = Cfg::kSmem;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -895,7 +942,8 @@ static cudaError_t max_clusters(K kernel, int slot, int sms, int* out) {
 }
 
 template <typename K, typename P>
-static cudaError_t launch_pairs(K kernel, const P& params, int clusters, cudaStream_t s) {
+static cudaError_t launch_pairs(K kernel, const P& params, int threads, int clusters,
+                                cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -904,7 +952,7 @@ static cudaError_t launch_pairs(K kernel, const P& params, int clusters, cudaStr
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.blockDim = dim3(Cfg::kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = Cfg::kSmem;
   cfg.stream = s;
   cfg.attrs = attr;
@@ -916,9 +964,10 @@ static cudaError_t launch_pairs(K kernel, const P& params, int clusters, cudaStr
 template <int STAGE>
 static cudaError_t launch_instance(const GemmLaunch& l, int pair_tiles, int sms, cudaStream_t s) {
   int n = 0;
-  const cudaError_t e = max_clusters(ns_gemm_kernel<STAGE>, STAGE, sms, &n);
+  const cudaError_t e = max_clusters(ns_gemm_kernel<STAGE>, STAGE, Cfg::kThreads, sms, &n);
   if (e != cudaSuccess) return e;
-  return launch_pairs(ns_gemm_kernel<STAGE>, l, pair_tiles < n ? pair_tiles : n, s);
+  return launch_pairs(ns_gemm_kernel<STAGE>, l, Cfg::kThreads, pair_tiles < n ? pair_tiles : n,
+                      s);
 }
 
 int gemm_smem_bytes() { return Cfg::kSmem; }
@@ -940,9 +989,10 @@ cudaError_t launch_gemm(const GemmLaunch& l, int stage, int pair_tiles, int sms,
 // other clusters.  The grid is therefore never larger than what fits.
 cudaError_t launch_rounds(const RoundsLaunch& l, int sms, cudaStream_t s) {
   int n = 0;
-  const cudaError_t e = max_clusters(ns_rounds_kernel, 3, sms, &n);
+  const cudaError_t e = max_clusters(ns_rounds_kernel, 3, Cfg::kRoundsThreads, sms, &n);
   if (e != cudaSuccess) return e;
-  return launch_pairs(ns_rounds_kernel, l, l.total_items < n ? l.total_items : n, s);
+  return launch_pairs(ns_rounds_kernel, l, Cfg::kRoundsThreads,
+                      l.total_items < n ? l.total_items : n, s);
 }
 
 }  // namespace muon
