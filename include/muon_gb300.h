@@ -74,8 +74,8 @@ typedef struct muon_group {
 typedef enum muon_kernel_kind {
   MUON_K_PROLOGUE = 0,   /* momentum, Nesterov blend, bf16 cast, norm partials  */
   MUON_K_SMALL_NS = 1,   /* whole step in fp32 for min(rows,cols) < 64          */
-  MUON_K_GRAM = 2,       /* A = s^2 X X^T, upper tiles + mirror                 */
-  MUON_K_POLY = 3,       /* B' = a I + b A + c A A, upper tiles + mirror        */
+  MUON_K_GRAM = 2,       /* A = s^2 X X^T, upper 256 x 256 tiles only           */
+  MUON_K_POLY = 3,       /* B' = a I + b A + c A A, upper 256 x 256 tiles only  */
   MUON_K_UPDATE = 4,     /* X <- s B' X  (= s (a X + B X))                      */
   MUON_K_APPLY = 5,      /* p <- (1 - lr wd) p - lr scale O (or O as bf16)      */
   MUON_K_ADAM = 6,       /* DistAdam update of non-matrix parameters            */
@@ -242,6 +242,21 @@ int muon_set_fused_ns(int enable);
  * -1 (nothing changed) if mode is not 0, 1 or 2.
  */
 int muon_set_persistent_rounds(int mode);
+
+/*
+ * Where the parameter write runs (no counterpart on the pages).  enable = 1
+ * (the default): when one persistent rounds launch (mode 1 or 2 above) covers
+ * every tensor-core matrix of a muon_step or muon_step_grouped call, every
+ * weight's cols is a multiple of 8, and rows and cols of every rows > cols
+ * weight are multiples of 8, the write is launched right behind the rounds
+ * kernel and runs beside its last round: its warps take the matrices in the
+ * order their last round ends (waiting, bounded, on the same completion
+ * counters), and that last round stores O of a rows > cols matrix already
+ * transposed.  enable = 0: the write runs after the rounds kernel.  Same
+ * results and workspace size either way; muon_ns5 always uses the second form.
+ * Process-wide; affects calls made afterwards.  Returns the previous setting.
+ */
+int muon_set_streamed_apply(int enable);
 
 /* Static English text for a status code. */
 const char* muon_status_string(muon_status status);

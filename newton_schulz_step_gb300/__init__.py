@@ -26,7 +26,7 @@ __all__ = [
     "GroupedStep", "AdamStep", "adam_step", "ADAM_LR", "ADAM_BETAS", "ADAM_EPS",
     "workspace_status", "status_string", "kernel_launch_count", "trace_begin", "trace_end",
     "set_fused_ns", "fused_ns", "set_persistent_rounds", "persistent_rounds",
-    "KERNEL_KINDS",
+    "set_streamed_apply", "streamed_apply", "KERNEL_KINDS",
 ]
 
 # Quintic coefficients and rounds as printed in "Muon Custom Sizing 实战", section 2.3.
@@ -112,6 +112,8 @@ def load_library():
     L.muon_set_persistent_rounds.restype = ci
     L.muon_set_fused_ns.argtypes = [ci]
     L.muon_set_fused_ns.restype = ci
+    L.muon_set_streamed_apply.argtypes = [ci]
+    L.muon_set_streamed_apply.restype = ci
     L.muon_status_string.argtypes = [ci]
     L.muon_status_string.restype = ctypes.c_char_p
     L.muon_kernel_launch_count.argtypes = []
@@ -427,6 +429,30 @@ class persistent_rounds:
 
     def __exit__(self, *exc):
         set_persistent_rounds(self.prev)
+        return False
+
+
+def set_streamed_apply(enable: bool) -> bool:
+    """Run the parameter write beside the persistent rounds kernel's last round (True,
+    the default, where the call allows it) or after it (False); returns the previous
+    value."""
+    return bool(load_library().muon_set_streamed_apply(int(bool(enable))))
+
+
+class streamed_apply:
+    """Context manager: `with streamed_apply(False): ...` runs the block with the
+    parameter write after the rounds kernel."""
+
+    def __init__(self, enable: bool):
+        self.enable = enable
+        self.prev = None
+
+    def __enter__(self):
+        self.prev = set_streamed_apply(self.enable)
+        return self
+
+    def __exit__(self, *exc):
+        set_streamed_apply(self.prev)
         return False
 
 

@@ -28,6 +28,7 @@ enum DeviceError : unsigned int {
   kErrTimeoutDrain = 8u,
   kErrTimeoutFused = 16u,
   kErrTimeoutDepend = 32u,
+  kErrTimeoutApply = 64u,
 };
 
 // What the prologue computes from (g, buf).
@@ -57,6 +58,7 @@ struct PrologueLaunch {
   int wait_prior;         // 1: block 0 waits for the preceding grid (PDL) before exiting
   unsigned int* zero;     // counters the launch zeroes (block 0), or null
   int n_zero;
+  unsigned int* zero_work;  // the streamed apply's claim counter, zeroed by block 0 (or null)
 };
 
 // One tensor-core group of the grouped apply launch: the NS result O (bf16,
@@ -70,12 +72,25 @@ struct ApplyGroup {
   int nparts;
   int block_begin;
   float lr_eff, decay;
+  // streamed form: O is in the parameter's orientation (r x c, row stride ldx),
+  // matrix z may be written once its completion counter done[done_begin + z]
+  // reaches done_target; its rows are split into units of unit_rows rows
+  int done_begin;
+  unsigned int done_target;
+  int unit_rows, units_per_mat;
+  int unit_begin;         // first work unit of this group
 };
 
 struct ApplyLaunch {
   ApplyGroup grp[kMaxPrologueGroups];
   int n_groups;
   int total_blocks;
+  // streamed form (apply_stream_kernel), launched beside the persistent rounds
+  // kernel: warps claim units in order from *work and wait for their matrix
+  const unsigned int* done;
+  unsigned int* work;
+  unsigned int* status;   // sticky device error word (a set word ends the waits)
+  int total_units;
 };
 
 // One group of the fp32 small-matrix path.
@@ -146,6 +161,8 @@ struct RoundsProblem {
   const float* parts;     // norm partials [batch, nparts]
   int nparts;
   int done_begin;         // this problem's first matrix counter
+  int o_pmajor;           // the last round stores O transposed (x_out_t): the parameter's
+                          // orientation of a rows > cols matrix, for the streamed apply
 };
 
 struct RoundsLaunch {
@@ -158,6 +175,8 @@ struct RoundsLaunch {
   CUtensorMap b_op[kMaxProblems];      // B' (box 64 x 128)
   CUtensorMap b_mn[kMaxProblems];      // B' read transposed (box 64 x 64)
   CUtensorMap b_out[kMaxProblems];     // B' 64 x 32 output blocks
+  CUtensorMap x_out_t[kMaxProblems];   // o_pmajor: O^T (n x m, row stride round_up(m, 8)) in
+                                       // the last round's output buffer, blocks of 64 rows x 32
   RoundsProblem prob[kMaxProblems];
   int n_prob;
   int steps;
@@ -227,6 +246,10 @@ struct AdamLaunch {
 cudaError_t launch_prologue(const PrologueLaunch& l, int mode, bool pdl, cudaStream_t s);
 cudaError_t launch_small(const SmallLaunch& l, int total_blocks, int max_mn, cudaStream_t s);
 cudaError_t launch_apply(const ApplyLaunch& l, bool to_param, cudaStream_t s);
+// The streamed parameter write (ApplyLaunch streamed fields), a programmatic
+// dependent of the persistent rounds kernel, `blocks` CTAs of 256 threads.
+cudaError_t launch_apply_stream(const ApplyLaunch& l, int blocks, cudaStream_t s);
+constexpr unsigned int kRoundsSignalsPerTile = 8;  // completion-counter adds per stored pair tile
 // One launch of a GEMM stage over `pair_tiles` cluster tiles (two 128 x 256
 // CTA tiles each); the grid is sized from the device's SM count.
 cudaError_t launch_gemm(const GemmLaunch& l, int stage, int pair_tiles, int sms, cudaStream_t s);

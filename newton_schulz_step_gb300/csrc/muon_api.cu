@@ -32,6 +32,12 @@ std::atomic<int> g_fused_enabled{1};
 // NS rounds of tensor-core groups: 0 one launch per stage and round, 1 one
 // persistent launch per chunk, 2 (default) persistent when a round is short
 std::atomic<int> g_rounds_enabled{2};
+// 1: the parameter write streams beside the persistent rounds kernel when one
+// such launch covers every tensor-core matrix of the call (apply_stream_kernel)
+std::atomic<int> g_stream_apply_enabled{1};
+// ... and only while the whole rounds launch is estimated under this (the
+// streamed write's waits give up after 2 s)
+constexpr double kStreamMaxUs = 1e5;
 
 // The persistent launch pays off while stage boundaries (launch, pipeline fill,
 // last-wave tail: a few microseconds each) weigh on a round; on rounds of
@@ -386,7 +392,7 @@ double round_mma_us(const std::vector<GPlan*>& chunk, int sms) {
 // tensor-core groups: every stage walks the groups by ascending n and each
 // group's matrices in order, so a matrix's next stage follows its current one.
 muon_status build_rounds(RoundsLaunch& R, const std::vector<GPlan*>& chunk, const Scalars& sc,
-                         uint8_t* ws) {
+                         uint8_t* ws, bool stream) {
   std::memset(&R, 0, sizeof(R));
   std::vector<GPlan*> order(chunk);
   std::stable_sort(order.begin(), order.end(),
@@ -410,7 +416,14 @@ muon_status build_rounds(RoundsLaunch& R, const std::vector<GPlan*>& chunk, cons
     P.parts = reinterpret_cast<const float*>(ws + g.parts);
     P.nparts = g.nparts;
     P.done_begin = g.ctr;
+    // the streamed apply reads O of a rows > cols matrix as O^T (n x m, row
+    // stride lda), written by the last round over that matrix's own X slot
+    // (the same size: m and n are multiples of 8)
+    P.o_pmajor = (stream && g.tall) ? 1 : 0;
     bool ok = true;
+    if (P.o_pmajor)
+      ok = make_tmap(&R.x_out_t[i], ws + ((sc.steps & 1) ? g.x1 : g.x0), g.m, g.n, g.batch, g.lda,
+                     32, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
     for (int b = 0; b < 2; ++b) {
       uint8_t* xb = ws + (b ? g.x1 : g.x0);
       ok = ok && operand_tmap(&R.x_op[i][b], xb, g.n, g.m, g.batch, g.ldx, kTileM) &&
@@ -535,6 +548,23 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
   std::vector<GPlan*> big;
   for (GPlan& g : gs)
     if (!g.small && g.batch > 0) big.push_back(&g);
+  std::vector<GPlan*> staged;
+  for (GPlan* g : big)
+    if (!is_fused(*g)) staged.push_back(g);
+  const int rounds_mode = g_rounds_enabled.load(std::memory_order_relaxed);
+  // -- the parameter write streams beside the rounds kernel when one persistent
+  //    launch covers every tensor-core matrix, every parameter row is whole
+  //    16-byte segments, and O^T of a rows > cols matrix fills its X slot exactly
+  bool stream = g_stream_apply_enabled.load(std::memory_order_relaxed) != 0 &&
+                sc.mode != kPrologueNsOnly && !big.empty() && staged.size() == big.size() &&
+                staged.size() <= static_cast<size_t>(kMaxProblems);
+  if (stream) {
+    const double round_us = round_mma_us(staged, sms);
+    stream = (rounds_mode == 1 || (rounds_mode == 2 && round_us < kPersistentRoundUs)) &&
+             round_us * sc.steps < kStreamMaxUs;
+    for (const GPlan* g : big)
+      if (g->c % 8 != 0 || (g->tall && (g->m % 8 != 0 || g->n % 8 != 0))) stream = false;
+  }
   for (size_t c0 = 0; c0 < big.size(); c0 += kMaxPrologueGroups) {
     PrologueLaunch pl;
     std::memset(&pl, 0, sizeof(pl));
@@ -567,6 +597,8 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
       int n = 0;
       for (const GPlan* g : big) n += g->batch;
       pl.n_zero = n;
+      // the streamed apply's claim counter: the status block's second word
+      if (stream) pl.zero_work = reinterpret_cast<unsigned int*>(ws) + 1;
     }
     const cudaError_t e = tracked_launch(st, {MUON_K_PROLOGUE, -1, 0.0, bytes},
                                          [&] { return launch_prologue(pl, sc.mode, pdl, st); });
@@ -620,10 +652,6 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
     if (s != MUON_OK) return s;
   }
 
-  std::vector<GPlan*> staged;
-  for (GPlan* g : big)
-    if (!is_fused(*g)) staged.push_back(g);
-  const int rounds_mode = g_rounds_enabled.load(std::memory_order_relaxed);
   for (size_t c0 = 0; c0 < staged.size(); c0 += kMaxProblems) {
     std::vector<GPlan*> chunk(staged.begin() + c0,
                               staged.begin() + std::min(staged.size(), c0 + kMaxProblems));
@@ -631,7 +659,7 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
         rounds_mode == 1 || (rounds_mode == 2 && round_mma_us(chunk, sms) < kPersistentRoundUs);
     if (persistent) {
       RoundsLaunch R;
-      s = build_rounds(R, chunk, sc, ws);
+      s = build_rounds(R, chunk, sc, ws, stream);
       if (s != MUON_OK) return s;
       if (R.total_items == 0) continue;
       double flops = 0;
@@ -665,6 +693,54 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
     }
   }
 
+  auto lr_eff = [&](const GPlan& g) {
+    const float scale = g.lr_scale > 0.f ? g.lr_scale
+                                         : static_cast<float>(std::sqrt(std::max(
+                                               1.0, static_cast<double>(g.r) / g.c)));
+    return sc.lr * scale;
+  };
+  if (stream) {
+    // -- apply, streamed: matrices in the order the rounds kernel finishes them
+    //    (ascending n, as build_rounds orders its problems)
+    std::vector<GPlan*> order(big);
+    std::stable_sort(order.begin(), order.end(),
+                     [](GPlan* x, GPlan* y) { return x->n < y->n; });
+    ApplyLaunch al;
+    std::memset(&al, 0, sizeof(al));
+    double bytes = 0;
+    int units = 0;
+    for (GPlan* gp : order) {
+      const GPlan& g = *gp;
+      ApplyGroup& ag = al.grp[al.n_groups++];
+      ag.o = reinterpret_cast<const __nv_bfloat16*>(ws + ((sc.steps & 1) ? g.x1 : g.x0));
+      ag.param = g.p;
+      ag.batch = g.batch;
+      ag.r = g.r;
+      ag.c = g.c;
+      ag.ldx = g.tall ? g.lda : g.ldx;  // O^T (n x m) or O = X (m x n)
+      ag.lr_eff = lr_eff(g);
+      ag.decay = 1.0f - sc.lr * sc.wd;
+      ag.done_begin = g.ctr;
+      unsigned int per_round = 0;
+      for (int stage = 0; stage < 3; ++stage)
+        per_round += static_cast<unsigned int>(stage_shape(g, stage).tiles_per_mat);
+      ag.done_target = static_cast<unsigned int>(sc.steps) * per_round * kRoundsSignalsPerTile;
+      ag.unit_rows = std::max(1, 8192 / g.c);
+      ag.units_per_mat = cdiv(g.r, ag.unit_rows);
+      ag.unit_begin = units;
+      units += g.batch * ag.units_per_mat;
+      bytes += static_cast<double>(g.batch) * g.r * g.c * 10.0;
+    }
+    al.total_units = units;
+    al.done = reinterpret_cast<const unsigned int*>(ws + kStatusBytes);
+    al.work = reinterpret_cast<unsigned int*>(ws) + 1;
+    al.status = reinterpret_cast<unsigned int*>(ws);
+    const int blocks = std::max(1, std::min(sms * 8, units));
+    const cudaError_t e = tracked_launch(st, {MUON_K_APPLY, -1, 0.0, bytes},
+                                         [&] { return launch_apply_stream(al, blocks, st); });
+    return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+  }
+
   // -- apply: p <- (1 - lr wd) p - lr rescale O (or O as bf16), one grouped launch;
   //    after round `steps` the result sits in X1 if steps is odd, else in X0
   for (size_t c0 = 0; c0 < big.size(); c0 += kMaxPrologueGroups) {
@@ -685,10 +761,7 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
       ag.ldx = g.ldx;
       ag.nparts = g.nparts;
       ag.block_begin = blocks;
-      const float scale = g.lr_scale > 0.f ? g.lr_scale
-                                            : static_cast<float>(std::sqrt(std::max(
-                                                  1.0, static_cast<double>(g.r) / g.c)));
-      ag.lr_eff = sc.lr * scale;
+      ag.lr_eff = lr_eff(g);
       ag.decay = 1.0f - sc.lr * sc.wd;
       blocks += g.batch * g.nparts;
       bytes += static_cast<double>(g.batch) * g.r * g.c *
@@ -924,6 +997,10 @@ const char* muon_status_string(muon_status status) {
 int muon_set_persistent_rounds(int enable) {
   if (enable < 0 || enable > 2) return -1;
   return g_rounds_enabled.exchange(enable);
+}
+
+int muon_set_streamed_apply(int enable) {
+  return g_stream_apply_enabled.exchange(enable ? 1 : 0);
 }
 
 int muon_set_fused_ns(int enable) {

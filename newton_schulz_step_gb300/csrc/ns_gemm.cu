@@ -80,6 +80,7 @@ struct Cfg {
   // completion-counter increments per stored pair tile: every epilogue warp of both CTAs
   static constexpr unsigned int kSignalsPerTile = 2 * kEpiWarps;
 };
+static_assert(Cfg::kSignalsPerTile == kRoundsSignalsPerTile, "the host computes the final counts");
 
 // Everything a role needs to know about one pair tile.
 struct TileCtx {
@@ -88,6 +89,7 @@ struct TileCtx {
   const CUtensorMap* b;    // operand B: K-major 64 x 128 (Gram, Poly) or 64 x 64 (Update, X)
   const CUtensorMap* bt;   // Poly: operand B read transposed, 64 x 64
   const CUtensorMap* out;  // output 32 x 64 blocks
+  const CUtensorMap* out_t;  // update: O^T in 64 x 32 blocks instead of `out` (or null)
   const CUtensorMap* in;   // Poly: A 32 x 64 blocks (the b A term)
   int mat, pr, tn;         // matrix, pair row (pr >= tiles_m: no rows), tile column
   int m, n, k_blocks;
@@ -369,6 +371,28 @@ __device__ bool epilogue_tile(const TileCtx& T, const GemmScalars& k, uint64_t* 
       if (lane == 0) ptx::bulk_wait_read<C::kSlots - 1>();
     }
     __syncwarp();
+    if (STAGE == kStageUpdate && T.out_t != nullptr) {
+      // O^T, the parameter's orientation of a rows > cols matrix: the block of
+      // rows j0.. (64) and columns i0.. (32), 64-byte rows, lane l writing
+      // column l (its TMEM row)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t v[32];
+        ptx::tmem_ld32_sync(tbase + static_cast<uint32_t>(u * 64 + h * 32), v);
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          *reinterpret_cast<__nv_bfloat16*>(blk + (32 * h + q) * 64 + lane * 2) =
+              __float2bfloat16_rn(s * __uint_as_float(v[q]));
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_3d(T.out_t, i0, j0, T.mat, blk);
+        ptx::bulk_commit();
+      }
+      es.slot ^= 1;
+      continue;
+    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint32_t v[32];
@@ -554,6 +578,7 @@ __device__ __forceinline__ TileCtx staged_ctx(const GemmLaunch& L, const Tile& t
   T.b = &L.tm_b[tl.prob];
   T.bt = &L.tm_bt[tl.prob];
   T.out = &L.tm_out[tl.prob];
+  T.out_t = nullptr;
   T.in = &L.tm_in[tl.prob];
   T.mat = tl.mat;
   T.pr = tl.pr;
@@ -696,6 +721,7 @@ __device__ __forceinline__ TileCtx rounds_ctx(const RoundsLaunch& L, const Item&
   const RoundsProblem& P = L.prob[it.p];
   const int cur = it.r & 1;
   TileCtx T;
+  T.out_t = nullptr;
   if (it.s == kStageGram) {          // A = s^2 X X^T
     T.a = &L.x_op[it.p][cur];
     T.at = nullptr;
@@ -717,6 +743,9 @@ __device__ __forceinline__ TileCtx rounds_ctx(const RoundsLaunch& L, const Item&
     T.bt = nullptr;
     T.out = &L.x_out[it.p][cur ^ 1];
     T.in = nullptr;
+    // the last round of a matrix whose O the streamed apply reads in the
+    // parameter's orientation
+    if (P.o_pmajor && it.r == L.steps - 1) T.out_t = &L.x_out_t[it.p];
   }
   T.mat = it.mat;
   T.pr = it.pr;
@@ -740,10 +769,13 @@ __global__ void __launch_bounds__(Cfg::kRoundsThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int rank = static_cast<int>(ptx::cluster_ctarank());
-  ptx::griddep_launch_dependents();
   const uint32_t tmem_base = setup_cta(sm, warp);
   // X0, the norm partials and the zeroed counters come from the prologue
   ptx::griddep_wait();
+  // the dependent (the streamed apply, which waits on this kernel's counters)
+  // may start once every CTA of this grid is resident, and after the prologue
+  // has completed (it zeroes the apply's claim counter)
+  ptx::griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {

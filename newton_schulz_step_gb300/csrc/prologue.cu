@@ -103,8 +103,10 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // completion counters of the persistent rounds kernel, which reads them only
   // after this grid has completed
-  if (blockIdx.x == 0)
+  if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < L.n_zero; i += blockDim.x) L.zero[i] = 0u;
+    if (threadIdx.x == 0 && L.zero_work != nullptr) *L.zero_work = 0u;
+  }
   int gi = 0;
   while (gi + 1 < L.n_groups && static_cast<int>(blockIdx.x) >= L.grp[gi + 1].block_begin) ++gi;
   const PrologueGroup& A = L.grp[gi];
@@ -301,6 +303,126 @@ __global__ void __launch_bounds__(256) apply_kernel(const __grid_constant__ Appl
   }
 }
 
+// ------------------------------------------------------------ streamed apply
+// The same parameter write, p <- (1 - lr wd) p - lr_eff O, launched as a
+// programmatic dependent of the persistent rounds kernel so that it runs
+// beside that kernel's last round: each block claims work units (a few rows
+// of one matrix, ~8192 elements) in the order the rounds kernel finishes
+// matrices, waits until the matrix's completion counter shows its last round
+// stored, and streams the rows.  O is already in the parameter's orientation
+// (the last round of a rows > cols matrix stores O^T), so every access is a
+// coalesced row access and the kernel needs almost no shared memory: one of
+// its blocks fits on an SM beside a rounds CTA.  Requires cols % 8 == 0
+// (16-byte row segments).
+constexpr int kStreamSeg = 8;    // elements per thread access (16 B of O, 32 B of p)
+constexpr int kStreamDepth = 4;  // row segments per thread in flight
+
+// Counter wait of the streamed apply: acquire, bounded, ended early by a set
+// status word.  One thread per block polls, with a backoff from 1 to 8 us:
+// the counters are the rounds kernel's own, which its epilogues update and
+// its scheduler warps poll, so these waits must not crowd their L2 lines.
+__device__ __forceinline__ bool wait_done(const unsigned int* p, unsigned int target,
+                                          const unsigned int* status) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  if (v >= target) return true;
+  unsigned long long t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  unsigned int sleep_ns = 1000;
+  while (true) {
+    __nanosleep(sleep_ns);
+    if (sleep_ns < 8000) sleep_ns *= 2;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return true;
+    if (*reinterpret_cast<const volatile unsigned int*>(status) != 0u) return false;
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > 2000000000ull) return false;
+  }
+}
+
+// (at most 85 registers: one block shares an SM with a rounds CTA)
+__global__ void __launch_bounds__(256, 3) apply_stream_kernel(const __grid_constant__ ApplyLaunch L) {
+  __shared__ int s_unit;
+  while (true) {
+    if (threadIdx.x == 0) {
+      int u = static_cast<int>(atomicAdd(L.work, 1u));
+      if (u < L.total_units) {
+        int gi = 0;
+        while (gi + 1 < L.n_groups && u >= L.grp[gi + 1].unit_begin) ++gi;
+        const ApplyGroup& A = L.grp[gi];
+        const int mat = (u - A.unit_begin) / A.units_per_mat;
+        if (!wait_done(L.done + A.done_begin + mat, A.done_target, L.status)) {
+          atomicOr(L.status, kErrTimeoutApply);
+          u = L.total_units;
+        }
+      }
+      s_unit = u;
+    }
+    __syncthreads();
+    const int u = s_unit;
+    __syncthreads();  // s_unit is rewritten by the next claim only after every thread read it
+    if (u >= L.total_units) break;
+    int gi = 0;
+    while (gi + 1 < L.n_groups && u >= L.grp[gi + 1].unit_begin) ++gi;
+    const ApplyGroup& A = L.grp[gi];
+    const int local = u - A.unit_begin;
+    const int mat = local / A.units_per_mat;
+    const int r0 = (local - mat * A.units_per_mat) * A.unit_rows;
+    const int r1 = min(A.r, r0 + A.unit_rows);
+    // every thread acquires the (already reached) count before reading O
+    asm volatile("{\n\t.reg .b32 t;\n\tld.acquire.gpu.global.u32 t, [%0];\n\t}" ::"l"(
+                     L.done + A.done_begin + mat)
+                 : "memory");
+    const size_t poff = static_cast<size_t>(mat) * A.r * A.c;
+    const size_t ooff = static_cast<size_t>(mat) * A.r * A.ldx;
+    const int segs_row = A.c / kStreamSeg;
+    const int segs = (r1 - r0) * segs_row;
+    for (int g0 = threadIdx.x; g0 < segs; g0 += blockDim.x * kStreamDepth) {
+      float4 pa[kStreamDepth], pb[kStreamDepth];
+      uint4 ow[kStreamDepth];
+      size_t pi[kStreamDepth];
+      bool in[kStreamDepth];
+#pragma unroll
+      for (int d = 0; d < kStreamDepth; ++d) {
+        const int g = g0 + static_cast<int>(blockDim.x) * d;
+        in[d] = g < segs;
+        const int row = r0 + (in[d] ? g / segs_row : 0);
+        const int col = in[d] ? (g - (row - r0) * segs_row) * kStreamSeg : 0;
+        pi[d] = poff + static_cast<size_t>(row) * A.c + col;
+        if (in[d]) {
+          pa[d] = __ldcs(reinterpret_cast<const float4*>(A.param + pi[d]));
+          pb[d] = __ldcs(reinterpret_cast<const float4*>(A.param + pi[d] + 4));
+          ow[d] = __ldcg(reinterpret_cast<const uint4*>(
+              A.o + ooff + static_cast<size_t>(row) * A.ldx + col));
+        }
+      }
+#pragma unroll
+      for (int d = 0; d < kStreamDepth; ++d) {
+        if (!in[d]) continue;
+        const uint32_t ws[4] = {ow[d].x, ow[d].y, ow[d].z, ow[d].w};
+        float o[kStreamSeg];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[h]));
+          o[2 * h] = f.x;
+          o[2 * h + 1] = f.y;
+        }
+        const float k = -A.lr_eff, dec = A.decay;
+        __stcs(reinterpret_cast<float4*>(A.param + pi[d]),
+               make_float4(fmaf(k, o[0], dec * pa[d].x), fmaf(k, o[1], dec * pa[d].y),
+                           fmaf(k, o[2], dec * pa[d].z), fmaf(k, o[3], dec * pa[d].w)));
+        __stcs(reinterpret_cast<float4*>(A.param + pi[d] + 4),
+               make_float4(fmaf(k, o[4], dec * pb[d].x), fmaf(k, o[5], dec * pb[d].y),
+                           fmaf(k, o[6], dec * pb[d].z), fmaf(k, o[7], dec * pb[d].w)));
+      }
+    }
+  }
+  // Programmatic dependent of the rounds kernel: the grid completes only after
+  // it (and so after everything before it in the stream)
+  if (blockIdx.x == 0 && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 template <int MODE>
 cudaError_t launch_mode(const PrologueLaunch& l, bool pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
@@ -330,6 +452,31 @@ cudaError_t launch_apply(const ApplyLaunch& l, bool to_param, cudaStream_t s) {
   cfg.numAttrs = 1;
   return to_param ? cudaLaunchKernelEx(&cfg, apply_kernel<true>, l)
                   : cudaLaunchKernelEx(&cfg, apply_kernel<false>, l);
+}
+
+cudaError_t launch_apply_stream(const ApplyLaunch& l, int blocks, cudaStream_t s) {
+  // shared memory is preferred over L1 (this kernel uses none) so that its
+  // blocks can share an SM with a rounds CTA configured for 227 KB
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(apply_stream_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, apply_stream_kernel, l);
 }
 
 cudaError_t launch_prologue(const PrologueLaunch& l, int mode, bool pdl, cudaStream_t s) {

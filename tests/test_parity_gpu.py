@@ -448,3 +448,82 @@ def test_device_timeout_is_reported_and_the_context_stays_usable():
     out = muon.ns5(G.to(DEV))                              # the context still works
     torch.cuda.synchronize()
     assert rel(f64(out[0]), oracle.newton_schulz5(f64(G[0]))) < NS_TOL
+
+
+# ------------------------------------------------------------ streamed parameter write
+# Shapes whose calls qualify for the parameter write beside the persistent rounds
+# kernel (every cols % 8 == 0; rows > cols ones with rows, cols % 8 == 0, whose last
+# round then stores O^T), and one call that does not (a rows > cols weight with
+# cols % 8 != 0) and falls back to the write after the rounds kernel.
+STREAM_CALLS = {
+    "wide+tall": [(3, 256, 640), (2, 768, 256)],
+    "tall-136": [(2, 200, 136), (1, 520, 136)],
+    "fallback": [(2, 300, 100), (1, 256, 640)],
+}
+
+
+def _stream_groups(shapes, seed):
+    out = []
+    for k, s in enumerate(shapes):
+        out.append((_rand(s, 0.02, torch.float32, seed + 3 * k),
+                    _rand(s, 1e-3, torch.bfloat16, seed + 3 * k + 1),
+                    _rand(s, 0.02, torch.float32, seed + 3 * k + 2)))
+    return out
+
+
+def _claims(step):
+    # the streamed write's claim counter: the second word of the workspace
+    return int(step.workspace.tensor[4:8].view(torch.int32).item())
+
+
+@pytest.mark.parametrize("call", list(STREAM_CALLS), ids=list(STREAM_CALLS))
+def test_streamed_apply_matches_the_write_after_the_rounds_and_the_oracle(call):
+    shapes = STREAM_CALLS[call]
+    host = _stream_groups(shapes, 70)
+    results = {}
+    for streamed in (True, False):
+        dev = [(p.to(DEV), g.to(DEV), b.to(DEV)) for p, g, b in host]
+        with muon.persistent_rounds(True), muon.streamed_apply(streamed):
+            step = muon.GroupedStep(dev, momentum=0.95, lr=0.02, weight_decay=0.01)
+            step()
+        torch.cuda.synchronize()
+        assert muon.workspace_status(step.workspace) == 0
+        results[streamed] = ([p.cpu() for p, _, _ in dev], [b.cpu() for _, _, b in dev],
+                             _claims(step))
+    # the same O and the same arithmetic: bit-identical either way
+    for a, b in zip(results[True][0], results[False][0]):
+        assert torch.equal(a, b)
+    for a, b in zip(results[True][1], results[False][1]):
+        assert torch.equal(a, b)
+    # the streamed write ran (its warps claimed every unit) only where the call qualifies
+    if call == "fallback":
+        assert results[True][2] == 0
+    else:
+        assert results[True][2] > 0
+    assert results[False][2] == 0
+    # and against the oracle: every matrix's update
+    for (p0, g0, b0), p1 in zip(host, results[True][0]):
+        for i in range(p0.shape[0]):
+            p_ref, _, _ = oracle.muon_step(f64(p0[i]), f64(g0[i]), f64(b0[i]), momentum=0.95,
+                                           lr=0.02, weight_decay=0.01)
+            upd = f64(p1[i]) - 0.9998 * f64(p0[i])
+            assert rel(upd, p_ref - 0.9998 * f64(p0[i])) < NS_TOL
+
+
+@pytest.mark.parametrize("steps", [1, 2, 5])
+def test_streamed_apply_with_other_round_counts(steps):
+    # the O buffer alternates with the round count; steps = 1 folds the norm into
+    # the transposed last-round store
+    host = _stream_groups([(2, 384, 128), (1, 128, 640)], 90)
+    dev = [(p.to(DEV), g.to(DEV), b.to(DEV)) for p, g, b in host]
+    with muon.persistent_rounds(True), muon.streamed_apply(True):
+        step = muon.GroupedStep(dev, momentum=0.9, lr=0.05, weight_decay=0.0, steps=steps)
+        step()
+    torch.cuda.synchronize()
+    assert muon.workspace_status(step.workspace) == 0
+    assert _claims(step) > 0
+    for (p0, g0, b0), (p1, _, _) in zip(host, dev):
+        for i in range(p0.shape[0]):
+            p_ref, _, _ = oracle.muon_step(f64(p0[i]), f64(g0[i]), f64(b0[i]), momentum=0.9,
+                                           lr=0.05, weight_decay=0.0, steps=steps)
+            assert rel(f64(p1[i]) - f64(p0[i]), p_ref - f64(p0[i])) < NS_TOL
