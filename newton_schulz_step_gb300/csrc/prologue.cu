@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(256) apply_kernel(const __grid_constant__ Appl
 // its blocks fits on an SM beside a rounds CTA.  Requires cols % 8 == 0
 // (16-byte row segments).
 constexpr int kStreamSeg = 8;    // elements per thread access (16 B of O, 32 B of p)
-constexpr int kStreamDepth = 4;  // row segments per thread in flight
+constexpr int kStreamDepth = 2;  // row segments per thread in flight
 
 // Counter wait of the streamed apply: acquire, bounded, ended early by a set
 // status word.  One thread per block polls, with a backoff from 1 to 8 us:
@@ -341,12 +341,16 @@ __device__ __forceinline__ bool wait_done(const unsigned int* p, unsigned int ta
   }
 }
 
-// (at most 85 registers: one block shares an SM with a rounds CTA)
-__global__ void __launch_bounds__(256, 3) apply_stream_kernel(const __grid_constant__ ApplyLaunch L) {
+// (at most 64 registers: four blocks per SM once the rounds kernel has left,
+// one beside a rounds CTA; measured faster than deeper, fewer blocks)
+__global__ void __launch_bounds__(256, 4) apply_stream_kernel(const __grid_constant__ ApplyLaunch L) {
   __shared__ int s_unit;
+  // thread 0 claims the block's next unit while the block works on the current one
+  unsigned int next = 0;
+  if (threadIdx.x == 0) next = atomicAdd(L.work, 1u);
   while (true) {
     if (threadIdx.x == 0) {
-      int u = static_cast<int>(atomicAdd(L.work, 1u));
+      int u = static_cast<int>(next);
       if (u < L.total_units) {
         int gi = 0;
         while (gi + 1 < L.n_groups && u >= L.grp[gi + 1].unit_begin) ++gi;
@@ -359,10 +363,13 @@ __global__ void __launch_bounds__(256, 3) apply_stream_kernel(const __grid_const
       }
       s_unit = u;
     }
+    // (thread 0's acquire of the counter and this barrier order the rounds
+    // kernel's stores of O before every thread's loads of it)
     __syncthreads();
     const int u = s_unit;
     __syncthreads();  // s_unit is rewritten by the next claim only after every thread read it
     if (u >= L.total_units) break;
+    if (threadIdx.x == 0) next = atomicAdd(L.work, 1u);
     int gi = 0;
     while (gi + 1 < L.n_groups && u >= L.grp[gi + 1].unit_begin) ++gi;
     const ApplyGroup& A = L.grp[gi];
@@ -370,10 +377,6 @@ __global__ void __launch_bounds__(256, 3) apply_stream_kernel(const __grid_const
     const int mat = local / A.units_per_mat;
     const int r0 = (local - mat * A.units_per_mat) * A.unit_rows;
     const int r1 = min(A.r, r0 + A.unit_rows);
-    // every thread acquires the (already reached) count before reading O
-    asm volatile("{\n\t.reg .b32 t;\n\tld.acquire.gpu.global.u32 t, [%0];\n\t}" ::"l"(
-                     L.done + A.done_begin + mat)
-                 : "memory");
     const size_t poff = static_cast<size_t>(mat) * A.r * A.c;
     const size_t ooff = static_cast<size_t>(mat) * A.r * A.ldx;
     const int segs_row = A.c / kStreamSeg;
