@@ -48,6 +48,8 @@ struct PrologueGroup {
   int batch, r, c, ldx;
   int nparts;             // blocks per matrix (<= kMaxParts)
   int block_begin;        // first block of this group in the launch
+  int pmajor;             // rows > cols, but X = u as is (the rounds kernel's first
+                          // round reads it transposed), row stride ldx
 };
 
 struct PrologueLaunch {
@@ -163,6 +165,8 @@ struct RoundsProblem {
   int done_begin;         // this problem's first matrix counter
   int o_pmajor;           // the last round stores O transposed (x_out_t): the parameter's
                           // orientation of a rows > cols matrix, for the streamed apply
+  int x0_u;               // X0 of this rows > cols matrix is u as stored (n x m, row stride
+                          // round_up(m, 8)): the first round reads it through u_mn / u_k
 };
 
 struct RoundsLaunch {
@@ -177,6 +181,8 @@ struct RoundsLaunch {
   CUtensorMap b_out[kMaxProblems];     // B' 64 x 32 output blocks
   CUtensorMap x_out_t[kMaxProblems];   // o_pmajor: O^T (n x m, row stride round_up(m, 8)) in
                                        // the last round's output buffer, blocks of 64 rows x 32
+  CUtensorMap u_mn[kMaxProblems];      // x0_u: u (n x m) as the Gram's MN-major operands (64 x 64)
+  CUtensorMap u_k[kMaxProblems];       // x0_u: u as the update's K-major operand B (64 x 128)
   RoundsProblem prob[kMaxProblems];
   int n_prob;
   int steps;

@@ -420,10 +420,15 @@ muon_status build_rounds(RoundsLaunch& R, const std::vector<GPlan*>& chunk, cons
     // stride lda), written by the last round over that matrix's own X slot
     // (the same size: m and n are multiples of 8)
     P.o_pmajor = (stream && g.tall) ? 1 : 0;
+    // ... and, likewise, that matrix's X0 is u as the prologue read it (n x m):
+    // the first round reads it transposed (no transpose in the prologue)
+    P.x0_u = P.o_pmajor;
     bool ok = true;
     if (P.o_pmajor)
       ok = make_tmap(&R.x_out_t[i], ws + ((sc.steps & 1) ? g.x1 : g.x0), g.m, g.n, g.batch, g.lda,
-                     32, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+                     32, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           operand_tmap(&R.u_mn[i], ws + g.x0, g.m, g.n, g.batch, g.lda, 64) &&
+           operand_tmap(&R.u_k[i], ws + g.x0, g.m, g.n, g.batch, g.lda, kTileM);
     for (int b = 0; b < 2; ++b) {
       uint8_t* xb = ws + (b ? g.x1 : g.x0);
       ok = ok && operand_tmap(&R.x_op[i][b], xb, g.n, g.m, g.batch, g.ldx, kTileM) &&
@@ -582,7 +587,10 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
       pg.batch = g.batch;
       pg.r = g.r;
       pg.c = g.c;
-      pg.ldx = g.ldx;
+      // a rows > cols matrix that the streamed rounds kernel reads as u: X0 = u
+      // as is, row stride lda (== its cols then)
+      pg.pmajor = (stream && g.tall) ? 1 : 0;
+      pg.ldx = pg.pmajor ? g.lda : g.ldx;
       pg.nparts = g.nparts;
       pg.block_begin = blocks;
       blocks += g.batch * g.nparts;

@@ -96,6 +96,10 @@ struct TileCtx {
   const float* parts;      // first round: norm partials of the batch
   int nparts;
   int first_round;
+  // first round of a rows > cols matrix whose X0 is u as stored: the Gram reads
+  // both operands MN-major through `at`/`bt`, the update operand B K-major
+  // through `b`
+  int x0_u;
 };
 
 struct GemmScalars {
@@ -113,6 +117,17 @@ __device__ __forceinline__ bool a_transposed(int pr, int kb) {
 template <int STAGE>
 __device__ __forceinline__ bool b_transposed(int pr, int kb) {
   return STAGE == kStagePoly && pr > (kb * kTileK) / 256;
+}
+
+// Operand majors of k-block kb of a tile.
+template <int STAGE>
+__device__ __forceinline__ bool a_mn_major(const TileCtx& T, int kb) {
+  return STAGE == kStageGram ? T.x0_u != 0 : a_transposed<STAGE>(T.pr, kb);
+}
+template <int STAGE>
+__device__ __forceinline__ bool b_mn_major(const TileCtx& T, int kb) {
+  if (STAGE == kStageUpdate) return T.x0_u == 0;
+  return STAGE == kStageGram ? T.x0_u != 0 : b_transposed<STAGE>(T.tn, kb);
 }
 
 __device__ __forceinline__ void record_failure(unsigned int* status, volatile int* abort_flag,
@@ -148,7 +163,7 @@ __device__ bool produce_tile(const TileCtx& T, uint8_t* smem, uint64_t* full, ui
     if (rank == 0) ptx::mbar_arrive_expect_tx(&full[ps.stage], 2 * C::kStageBytes);
     // operand A: this CTA's 128 rows x 64 k-columns, or (below the stored
     // tiles) the 64 x 128 block at the transposed position, MN-major
-    if (a_transposed<STAGE>(T.pr, kb)) {
+    if (a_mn_major<STAGE>(T, kb)) {
 #pragma unroll
       for (int q = 0; q < 2; ++q)
         ptx::tma_load_3d_pair(sa + q * (64 * kTileK * 2), T.at, tm * kTileM + q * 64,
@@ -156,18 +171,14 @@ __device__ bool produce_tile(const TileCtx& T, uint8_t* smem, uint64_t* full, ui
     } else {
       ptx::tma_load_3d_pair(sa, T.a, kb * kTileK, tm * kTileM, T.mat, bar);
     }
-    if (STAGE >= kStageUpdate) {
-      // operand B = X[k][j], MN-major: this CTA's 128 columns as 2 slabs of
-      // 64 columns x 64 k-rows
+    if (b_mn_major<STAGE>(T, kb)) {
+      // operand B = X[k][j] (update), or the transposed block (Poly below the
+      // stored tiles, a first-round Gram of u), MN-major: this CTA's 128
+      // columns as 2 slabs of 64 columns x 64 k-rows
+      const CUtensorMap* map = STAGE >= kStageUpdate ? T.b : T.bt;
 #pragma unroll
       for (int q = 0; q < 2; ++q)
-        ptx::tma_load_3d_pair(sb + q * (64 * kTileK * 2), T.b, T.tn * C::kBN + rank * 128 + q * 64,
-                              kb * kTileK, T.mat, bar);
-    } else if (b_transposed<STAGE>(T.tn, kb)) {
-      // Poly, below the stored tiles: the transposed block, MN-major
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
-        ptx::tma_load_3d_pair(sb + q * (64 * kTileK * 2), T.bt,
+        ptx::tma_load_3d_pair(sb + q * (64 * kTileK * 2), map,
                               T.tn * C::kBN + rank * kTileM + q * 64, kb * kTileK, T.mat, bar);
     } else {
       // operand B: this CTA's 128 of the tile column's 256 rows, K-major
@@ -207,7 +218,6 @@ __device__ bool mma_tile(const TileCtx& T, uint8_t* smem, uint64_t* full, uint64
                          uint64_t* acc_full, uint64_t* acc_empty, uint32_t tmem_base,
                          MmaState& ms, volatile int* abort_flag) {
   using C = Cfg;
-  constexpr bool kBmn = (STAGE >= kStageUpdate);
   // both CTAs' epilogues have drained this accumulator
   if (!ptx::mbar_wait(&acc_empty[ms.acc], ms.acc_phase ^ 1u, abort_flag)) return false;
   ptx::tc_fence_after();
@@ -218,8 +228,8 @@ __device__ bool mma_tile(const TileCtx& T, uint8_t* smem, uint64_t* full, uint64
     if (!ptx::mbar_wait(&full[ms.stage], ms.phase, abort_flag)) return false;
     const uint32_t sa = ptx::smem_u32(smem + ms.stage * C::kStageBytes);
     const uint32_t sb = sa + C::kABytes;
-    const bool a_mn = a_transposed<STAGE>(T.pr, kb);
-    const bool b_mn = kBmn || b_transposed<STAGE>(T.tn, kb);
+    const bool a_mn = a_mn_major<STAGE>(T, kb);
+    const bool b_mn = b_mn_major<STAGE>(T, kb);
     const uint32_t idesc = ptx::idesc_bf16(2 * kTileM, C::kBN, b_mn, a_mn);
 #pragma unroll
     for (int k = 0; k < kTileK / 16; ++k) {
@@ -589,6 +599,7 @@ __device__ __forceinline__ TileCtx staged_ctx(const GemmLaunch& L, const Tile& t
   T.parts = P.parts;
   T.nparts = P.nparts;
   T.first_round = P.first_round;
+  T.x0_u = 0;
   return T;
 }
 
@@ -756,6 +767,13 @@ __device__ __forceinline__ TileCtx rounds_ctx(const RoundsLaunch& L, const Item&
   T.parts = P.parts;
   T.nparts = P.nparts;
   T.first_round = it.r == 0 ? 1 : 0;
+  T.x0_u = (it.r == 0 && P.x0_u) ? 1 : 0;
+  if (T.x0_u && it.s == kStageGram) {
+    T.at = &L.u_mn[it.p];
+    T.bt = &L.u_mn[it.p];
+  } else if (T.x0_u && it.s == kStageUpdate) {
+    T.b = &L.u_k[it.p];
+  }
   return T;
 }
 

@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
   const int mat = local / A.nparts;
   const int part = local - mat * A.nparts;
   const int r = A.r, c = A.c;
-  const bool tall = r > c;
+  const bool tall = r > c && !A.pmajor;  // X = u^T, transposed here
   const int tiles_c = (c + 63) / 64;
   const int ntiles = ((r + 63) / 64) * tiles_c;
   const size_t moff = static_cast<size_t>(mat) * r * c;

@@ -58,14 +58,18 @@ def _rand(shape, std, dtype, seed):
 # ------------------------------------------------------------ intermediate buffers
 @pytest.mark.parametrize("shape,gdt", [((2, 256, 384), torch.bfloat16),
                                        ((1, 300, 520), torch.float32),
-                                       ((2, 520, 300), torch.bfloat16)])
+                                       ((2, 520, 300), torch.bfloat16),
+                                       ((2, 520, 304), torch.bfloat16)])
 @pytest.mark.parametrize("rounds", [False, True], ids=["per-stage", "persistent"])
 def test_prologue_writes_u_then_gram_and_poly(shape, gdt, rounds):
     """steps=1 leaves X0 = bf16(u or u^T), A = s^2 X0 X0^T and B' = aI + bA + cA^2 in the workspace.
 
     (The polynomial stage folds the a X term of the update into its output, so
     the update is the single product B' X.  A and B' are symmetric and only their
-    256 x 256 tiles on or above the diagonal are stored; those are compared.)"""
+    256 x 256 tiles on or above the diagonal are stored; those are compared.
+    A rows > cols matrix with rows and cols multiples of 8 under the persistent
+    rounds kernel keeps X0 = u as stored, n x m: that kernel's first round reads
+    it transposed.)"""
     b, r, c = shape
     m, n = min(r, c), max(r, c)
     ldx, lda = (n + 7) // 8 * 8, (m + 7) // 8 * 8
@@ -84,7 +88,11 @@ def test_prologue_writes_u_then_gram_and_poly(shape, gdt, rounds):
     x0_bytes = b * m * ldx * 2
     x0_off = 256 + (b * 4 + 255) // 256 * 256      # after the status block and the counters
     a_off = x0_off + 2 * ((x0_bytes + 255) // 256 * 256)
-    X0 = raw[x0_off:x0_off + x0_bytes].view(torch.bfloat16).view(b, m, ldx)[:, :, :n]
+    u_stored = rounds and r > c and r % 8 == 0 and c % 8 == 0
+    if u_stored:
+        X0 = raw[x0_off:x0_off + x0_bytes].view(torch.bfloat16).view(b, n, lda)[:, :, :m]
+    else:
+        X0 = raw[x0_off:x0_off + x0_bytes].view(torch.bfloat16).view(b, m, ldx)[:, :, :n]
     A = raw[a_off:a_off + b * m * lda * 2].view(torch.bfloat16).view(b, m, lda)[:, :, :m]
     a_bytes = (b * m * lda * 2 + 255) // 256 * 256
     Bm = raw[a_off + a_bytes:a_off + a_bytes + b * m * lda * 2].view(torch.bfloat16).view(b, m, lda)[:, :, :m]
@@ -93,8 +101,8 @@ def test_prologue_writes_u_then_gram_and_poly(shape, gdt, rounds):
         u = oracle.nesterov_blend(f64(g[i]), buf, 0.9)
         X = u.T if r > c else u
         assert rel(f64(mg[i]), buf) < EW_TOL
-        assert rel(f64(X0[i]), X) < 8e-3        # one bf16 rounding
-        x = f64(X0[i])
+        assert rel(f64(X0[i]), u if u_stored else X) < 8e-3        # one bf16 rounding
+        x = f64(X0[i]).T if u_stored else f64(X0[i])
         s = 1.0 / (np.linalg.norm(u) + 1e-7)
         A_ref = s * s * (x @ x.T)
         tiles = np.arange(m) // 256
