@@ -22,6 +22,7 @@ namespace muon {
 namespace {
 
 constexpr int kSmallThreads = 256;
+constexpr int kBatch = 8;  // elements per thread in flight in the elementwise passes
 constexpr int kSmallLd = 64;  // shared A, B are 64 x 64 with zero padding
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
@@ -80,22 +81,37 @@ __global__ void __launch_bounds__(kSmallThreads) small_ns_kernel(
   const int warp = tid >> 5, lane = tid & 31;
   const float beta = L.beta;
 
-  // 1. momentum, Nesterov blend, X = u (transposed when tall), sum(u^2)
+  // 1. momentum, Nesterov blend, X = u (transposed when tall), sum(u^2); the
+  //    loads of kBatch elements per thread are issued before any use, so the
+  //    pass costs a few memory latencies rather than one per element
   float ss = 0.f;
-  for (int e = tid; e < total; e += kSmallThreads) {
-    const int ri = e / c, ci = e - ri * c;
-    const float g = (G.gdt == MUON_BF16)
-                        ? __bfloat162float(static_cast<const __nv_bfloat16*>(G.g)[moff + e])
-                        : static_cast<const float*>(G.g)[moff + e];
-    float u = g;
-    if (MODE != kPrologueNsOnly) {
-      const float b = G.buf[moff + e];
-      const float nb = fmaf(1.0f - beta, g - b, b);
-      G.buf[moff + e] = nb;
-      u = (MODE == kPrologueNesterov) ? fmaf(beta, nb - g, g) : nb;
+  for (int e0 = tid; e0 < total; e0 += kSmallThreads * kBatch) {
+    float gv[kBatch], bv[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int e = e0 + k * kSmallThreads;
+      gv[k] = bv[k] = 0.f;
+      if (e < total) {
+        gv[k] = (G.gdt == MUON_BF16)
+                    ? __bfloat162float(static_cast<const __nv_bfloat16*>(G.g)[moff + e])
+                    : static_cast<const float*>(G.g)[moff + e];
+        if (MODE != kPrologueNsOnly) bv[k] = G.buf[moff + e];
+      }
     }
-    X[tall ? static_cast<size_t>(ci) * n + ri : static_cast<size_t>(ri) * n + ci] = u;
-    ss = fmaf(u, u, ss);
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int e = e0 + k * kSmallThreads;
+      if (e >= total) break;
+      const int ri = e / c, ci = e - ri * c;
+      float u = gv[k];
+      if (MODE != kPrologueNsOnly) {
+        const float nb = fmaf(1.0f - beta, gv[k] - bv[k], bv[k]);
+        G.buf[moff + e] = nb;
+        u = (MODE == kPrologueNesterov) ? fmaf(beta, nb - gv[k], gv[k]) : nb;
+      }
+      X[tall ? static_cast<size_t>(ci) * n + ri : static_cast<size_t>(ri) * n + ci] = u;
+      ss = fmaf(u, u, ss);
+    }
   }
   for (int e = tid; e < kSmallLd * kSmallLd; e += kSmallThreads) {
     As[e] = 0.f;
@@ -140,14 +156,29 @@ __global__ void __launch_bounds__(kSmallThreads) small_ns_kernel(
     __syncthreads();
   }
 
-  // apply (or write the bf16 result), in the input's orientation
-  for (int e = tid; e < total; e += kSmallThreads) {
-    const int ri = e / c, ci = e - ri * c;
-    const float o = X[tall ? static_cast<size_t>(ci) * n + ri : static_cast<size_t>(ri) * n + ci];
-    if (MODE == kPrologueNsOnly)
-      G.out[moff + e] = __float2bfloat16_rn(o);
-    else
-      G.param[moff + e] = fmaf(-G.lr_eff, o, L.decay * G.param[moff + e]);
+  // apply (or write the bf16 result), in the input's orientation, kBatch
+  // parameter loads per thread in flight
+  for (int e0 = tid; e0 < total; e0 += kSmallThreads * kBatch) {
+    float pv[kBatch];
+    if (MODE != kPrologueNsOnly) {
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int e = e0 + k * kSmallThreads;
+        pv[k] = e < total ? G.param[moff + e] : 0.f;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int e = e0 + k * kSmallThreads;
+      if (e >= total) break;
+      const int ri = e / c, ci = e - ri * c;
+      const float o =
+          X[tall ? static_cast<size_t>(ci) * n + ri : static_cast<size_t>(ri) * n + ci];
+      if (MODE == kPrologueNsOnly)
+        G.out[moff + e] = __float2bfloat16_rn(o);
+      else
+        G.param[moff + e] = fmaf(-G.lr_eff, o, L.decay * pv[k]);
+    }
   }
 }
 
