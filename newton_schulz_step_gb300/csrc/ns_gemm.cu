@@ -24,7 +24,7 @@
 // MN-major.
 //
 // Kernel shape: persistent clusters of two CTAs (a CTA pair), one CTA per SM,
-// 192 threads:
+// 192 threads (224 in the rounds kernel, whose warp 6 schedules, below):
 //   warp 0      TMA producer (one lane) into a ring of swizzled smem stages
 //   warp 1      TMEM allocator; in the even CTA also the tcgen05.mma issuer
 //   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator, fp32 math, 32 x 64
