@@ -499,12 +499,19 @@ def traffic_for(kernel: str, workload: str):
 
 
 def source_hash(kernel: str):
+    """Hash of a kernel's sources with comments and blank space removed, so that a
+    recorded ncu capture stays valid across comment edits but not code changes."""
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "newton_schulz_step_gb300", "csrc")
     for f in KERNEL_SOURCES.get(kernel, tuple(sorted(os.listdir(csrc)))):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        text = " ".join(text.split())
+        h.update(f.encode() + text.encode())
     return h.hexdigest()[:16]
 
 
