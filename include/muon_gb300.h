@@ -245,15 +245,17 @@ int muon_set_persistent_rounds(int mode);
 
 /*
  * Where the parameter write runs (no counterpart on the pages).  enable = 1
- * (the default): when one persistent rounds launch (mode 1 or 2 above) covers
- * every tensor-core matrix of a muon_step or muon_step_grouped call, every
- * weight's cols is a multiple of 8, and rows and cols of every rows > cols
- * weight are multiples of 8, the write is launched right behind the rounds
- * kernel and runs beside its last round: its warps take the matrices in the
- * order their last round ends (waiting, bounded, on the same completion
- * counters), and that last round stores O of a rows > cols matrix already
- * transposed.  enable = 0: the write runs after the rounds kernel.  Same
- * results and workspace size either way; muon_ns5 always uses the second form.
+ * (the default): when every tensor-core matrix of a muon_step or
+ * muon_step_grouped call goes through one staged NS chain (one persistent
+ * rounds launch, or one launch per stage and round; see above), every weight's
+ * cols is a multiple of 8, and rows and cols of every rows > cols weight are
+ * multiples of 8, the write is launched right behind the last update (the
+ * rounds kernel, or the last round's update launch) and runs beside it: its
+ * blocks take the matrices in the order that update ends them (waiting,
+ * bounded, on per-matrix completion counters), and the last round stores O of
+ * a rows > cols matrix already transposed.  enable = 0: the write runs after
+ * the NS.  Same results and workspace size either way; muon_ns5 always uses
+ * the second form.
  * Process-wide; affects calls made afterwards.  Returns the previous setting.
  */
 int muon_set_streamed_apply(int enable);

@@ -130,6 +130,10 @@ struct GemmProblem {
   int nparts;
   int first_round;              // fold s = 1/(||u||_F + eps) in
   int reverse;                  // walk this problem's matrices in descending order
+  // last update before a streamed parameter write (GemmLaunch::done set): the
+  // problem's first matrix counter, and whether O goes out transposed (tm_out_t)
+  int done_begin;
+  int o_pmajor;
 };
 
 struct GemmLaunch {
@@ -139,11 +143,16 @@ struct GemmLaunch {
   CUtensorMap tm_bt[kMaxProblems];  // Poly: symmetric operand B read transposed (box 64 x 64)
   CUtensorMap tm_out[kMaxProblems]; // output blocks (box 64 x 32 bf16, 128-byte swizzle)
   CUtensorMap tm_in[kMaxProblems];  // Poly: blocks of A for the b A term (box 64 x 32, 128-byte swizzle)
+  CUtensorMap tm_out_t[kMaxProblems];  // o_pmajor: O^T blocks of 64 rows x 32 (as x_out_t below)
   GemmProblem prob[kMaxProblems];
   int n_prob;
   int total_tiles;                  // pair tiles
   float a, b, c, eps;
   unsigned int* status;             // sticky device error word
+  // update launch of the last round with the parameter write streamed beside it:
+  // per-matrix completion counters (zeroed by the prologue), advanced like the
+  // rounds kernel's, which the write waits on; null otherwise
+  unsigned int* done;
 };
 
 enum GemmStage : int { kStageGram = 0, kStagePoly = 1, kStageUpdate = 2 };

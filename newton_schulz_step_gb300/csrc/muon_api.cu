@@ -308,8 +308,11 @@ double stage_flops(const GPlan& g, int stage) {
 
 // Builds the launch block of one stage for a chunk of tensor-core groups.
 // `cur` selects X0 (0) or X1 (1) as this round's X.
+// `signal`: the last round's update, with the parameter write streamed beside
+// it: per-matrix completion counters, and O^T for rows > cols matrices.
 muon_status build_gemm(GemmLaunch& L, const std::vector<GPlan*>& chunk, int stage,
-                       int cur, bool first_round, const Scalars& sc, uint8_t* ws) {
+                       int cur, bool first_round, const Scalars& sc, uint8_t* ws,
+                       bool signal) {
   std::memset(&L, 0, sizeof(L));
   // Order of the tile walk.  The update and Poly stages walk the groups by
   // ascending n (matrices ascending); the Gram stage walks the exact reverse,
@@ -362,6 +365,13 @@ muon_status build_gemm(GemmLaunch& L, const std::vector<GPlan*>& chunk, int stag
            operand_tmap(&L.tm_at[i], ws + g.bm, g.m, g.m, g.batch, g.lda, 64) &&
            operand_tmap(&L.tm_b[i], xc, g.n, g.m, g.batch, g.ldx, 64) &&
            output_tmap(&L.tm_out[i], xn, g.n, g.m, g.batch, g.ldx);
+      if (signal) {
+        P.done_begin = g.ctr;
+        P.o_pmajor = g.tall ? 1 : 0;
+        if (g.tall)
+          ok = ok && make_tmap(&L.tm_out_t[i], xn, g.m, g.n, g.batch, g.lda, 32, 64,
+                               CU_TENSOR_MAP_SWIZZLE_NONE);
+      }
     }
     if (!ok) return MUON_ERR_CUDA;
   }
@@ -372,6 +382,7 @@ muon_status build_gemm(GemmLaunch& L, const std::vector<GPlan*>& chunk, int stag
   L.c = sc.c;
   L.eps = sc.eps;
   L.status = reinterpret_cast<unsigned int*>(ws);
+  if (signal) L.done = reinterpret_cast<unsigned int*>(ws + kStatusBytes);
   return MUON_OK;
 }
 
@@ -557,19 +568,25 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
   for (GPlan* g : big)
     if (!is_fused(*g)) staged.push_back(g);
   const int rounds_mode = g_rounds_enabled.load(std::memory_order_relaxed);
-  // -- the parameter write streams beside the rounds kernel when one persistent
-  //    launch covers every tensor-core matrix, every parameter row is whole
-  //    16-byte segments, and O^T of a rows > cols matrix fills its X slot exactly
+  // -- the parameter write streams beside the last update (the persistent rounds
+  //    kernel, or the last round's update launch) when one such chunk covers
+  //    every tensor-core matrix, every parameter row is whole 16-byte segments,
+  //    and O^T of a rows > cols matrix fills its X slot exactly
   bool stream = g_stream_apply_enabled.load(std::memory_order_relaxed) != 0 &&
                 sc.mode != kPrologueNsOnly && !big.empty() && staged.size() == big.size() &&
                 staged.size() <= static_cast<size_t>(kMaxProblems);
+  bool stream_rounds = false;  // ... beside the persistent rounds kernel
   if (stream) {
     const double round_us = round_mma_us(staged, sms);
-    stream = (rounds_mode == 1 || (rounds_mode == 2 && round_us < kPersistentRoundUs)) &&
-             round_us * sc.steps < kStreamMaxUs;
+    stream_rounds = rounds_mode == 1 || (rounds_mode == 2 && round_us < kPersistentRoundUs);
+    // (the write's waits give up after 2 s: beside the rounds kernel they span
+    // all its rounds, beside the last update launch only that launch, which is
+    // bounded here by a whole round)
+    if ((stream_rounds ? round_us * sc.steps : round_us) >= kStreamMaxUs) stream = false;
     for (const GPlan* g : big)
       if (g->c % 8 != 0 || (g->tall && (g->m % 8 != 0 || g->n % 8 != 0))) stream = false;
   }
+  stream_rounds = stream && stream_rounds;
   for (size_t c0 = 0; c0 < big.size(); c0 += kMaxPrologueGroups) {
     PrologueLaunch pl;
     std::memset(&pl, 0, sizeof(pl));
@@ -589,7 +606,7 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
       pg.c = g.c;
       // a rows > cols matrix that the streamed rounds kernel reads as u: X0 = u
       // as is, row stride lda (== its cols then)
-      pg.pmajor = (stream && g.tall) ? 1 : 0;
+      pg.pmajor = (stream_rounds && g.tall) ? 1 : 0;
       pg.ldx = pg.pmajor ? g.lda : g.ldx;
       pg.nparts = g.nparts;
       pg.block_begin = blocks;
@@ -667,7 +684,7 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
         rounds_mode == 1 || (rounds_mode == 2 && round_mma_us(chunk, sms) < kPersistentRoundUs);
     if (persistent) {
       RoundsLaunch R;
-      s = build_rounds(R, chunk, sc, ws, stream);
+      s = build_rounds(R, chunk, sc, ws, stream_rounds);
       if (s != MUON_OK) return s;
       if (R.total_items == 0) continue;
       double flops = 0;
@@ -685,7 +702,8 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
       const int stages[3] = {kStageGram, kStagePoly, kStageUpdate};
       for (int stage : stages) {
         GemmLaunch L;
-        s = build_gemm(L, chunk, stage, cur, first, sc, ws);
+        s = build_gemm(L, chunk, stage, cur, first, sc, ws,
+                       stream && it == sc.steps - 1 && stage == kStageUpdate);
         if (s != MUON_OK) return s;
         if (L.total_tiles == 0) continue;
         double flops = 0;
@@ -732,7 +750,12 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
       unsigned int per_round = 0;
       for (int stage = 0; stage < 3; ++stage)
         per_round += static_cast<unsigned int>(stage_shape(g, stage).tiles_per_mat);
-      ag.done_target = static_cast<unsigned int>(sc.steps) * per_round * kRoundsSignalsPerTile;
+      // the value the counter ends with: every tile of every round (rounds
+      // kernel) or of the last update launch
+      ag.done_target = (stream_rounds ? static_cast<unsigned int>(sc.steps) * per_round
+                                      : static_cast<unsigned int>(
+                                            stage_shape(g, kStageUpdate).tiles_per_mat)) *
+                       kRoundsSignalsPerTile;
       ag.unit_rows = std::max(1, 8192 / g.c);
       ag.units_per_mat = cdiv(g.r, ag.unit_rows);
       ag.unit_begin = units;

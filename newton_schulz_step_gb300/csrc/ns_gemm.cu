@@ -590,7 +590,8 @@ __device__ __forceinline__ TileCtx staged_ctx(const GemmLaunch& L, const Tile& t
   T.b = &L.tm_b[tl.prob];
   T.bt = &L.tm_bt[tl.prob];
   T.out = &L.tm_out[tl.prob];
-  T.out_t = nullptr;
+  // (o_pmajor only on the last update before a streamed parameter write)
+  T.out_t = P.o_pmajor ? &L.tm_out_t[tl.prob] : nullptr;
   T.in = &L.tm_in[tl.prob];
   T.mat = tl.mat;
   T.pr = tl.pr;
@@ -660,11 +661,22 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     const GemmScalars k{L.a, L.b, L.c, L.eps};
     EpiState es;
     for (int t = first_tile(); t < L.total_tiles; t += tile_stride()) {
-      const TileCtx T = staged_ctx(L, decode_tile<STAGE>(L, t));
+      const Tile tl = decode_tile<STAGE>(L, t);
+      const TileCtx T = staged_ctx(L, tl);
       if (!epilogue_tile<STAGE>(T, k, sm.acc_full, sm.acc_empty, my_in, my_slots, tmem_base, es,
                                 sm.abort_flag, quarter, lane, rank, nullptr, 0u)) {
         record_failure(L.status, sm.abort_flag, kErrTimeoutEpilogue);
         break;
+      }
+      // last update before a streamed parameter write: this warp's blocks of
+      // the tile are in global memory, count them for the write
+      if (STAGE == kStageUpdate && L.done != nullptr) {
+        if (lane == 0) {
+          ptx::bulk_wait<0>();
+          ptx::fence_proxy_async_global();
+          ptx::red_release_gpu_add(L.done + L.prob[tl.prob].done_begin + tl.mat, 1u);
+        }
+        __syncwarp();
       }
     }
     // all bulk copies of this warp are complete before the CTA exits

@@ -484,14 +484,16 @@ def _claims(step):
     return int(step.workspace.tensor[4:8].view(torch.int32).item())
 
 
+@pytest.mark.parametrize("rounds", [True, False], ids=["persistent", "per-stage"])
 @pytest.mark.parametrize("call", list(STREAM_CALLS), ids=list(STREAM_CALLS))
-def test_streamed_apply_matches_the_write_after_the_rounds_and_the_oracle(call):
+def test_streamed_apply_matches_the_write_after_the_rounds_and_the_oracle(call, rounds):
+    # beside the persistent rounds kernel, or beside the last round's update launch
     shapes = STREAM_CALLS[call]
     host = _stream_groups(shapes, 70)
     results = {}
     for streamed in (True, False):
         dev = [(p.to(DEV), g.to(DEV), b.to(DEV)) for p, g, b in host]
-        with muon.persistent_rounds(True), muon.streamed_apply(streamed):
+        with muon.persistent_rounds(rounds), muon.streamed_apply(streamed):
             step = muon.GroupedStep(dev, momentum=0.95, lr=0.02, weight_decay=0.01)
             step()
         torch.cuda.synchronize()
@@ -518,13 +520,14 @@ def test_streamed_apply_matches_the_write_after_the_rounds_and_the_oracle(call):
             assert rel(upd, p_ref - 0.9998 * f64(p0[i])) < NS_TOL
 
 
+@pytest.mark.parametrize("rounds", [True, False], ids=["persistent", "per-stage"])
 @pytest.mark.parametrize("steps", [1, 2, 5])
-def test_streamed_apply_with_other_round_counts(steps):
+def test_streamed_apply_with_other_round_counts(steps, rounds):
     # the O buffer alternates with the round count; steps = 1 folds the norm into
     # the transposed last-round store
     host = _stream_groups([(2, 384, 128), (1, 128, 640)], 90)
     dev = [(p.to(DEV), g.to(DEV), b.to(DEV)) for p, g, b in host]
-    with muon.persistent_rounds(True), muon.streamed_apply(True):
+    with muon.persistent_rounds(rounds), muon.streamed_apply(True):
         step = muon.GroupedStep(dev, momentum=0.9, lr=0.05, weight_decay=0.0, steps=steps)
         step()
     torch.cuda.synchronize()
