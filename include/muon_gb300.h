@@ -8,9 +8,9 @@
  *         five rounds) and section 四 (momentum lerp, Nesterov blend, decoupled
  *         decay lr*wd, write-back with alpha = -lr * max(1, hdim/dim)^0.5);
  *   [PG]  "parameter-golf train_gpt.py 源码精读：Muon 优化器、Int8 量化与 DDP 数据
- *         加载全解", part 1, section 核心思想 (zeropower_via_newtonschulz5:
+ *         加载全解", part 1, section 核心思想 (the Newton-Schulz function:
  *         X /= ||X||; repeat A = X X^T, B = bA + cA^2, X = aX + BX) and section
- *         分布式细节 (rescale g *= max(1, m/n)^0.5).
+ *         分布式细节 (rescale of the result by max(1, m/n)^0.5).
  *
  * Conventions shared by every entry point:
  *   - Matrices are row-major and contiguous, stacked as [batch, rows, cols].
@@ -93,7 +93,7 @@ size_t muon_workspace_bytes(int batch, int rows, int cols);
 size_t muon_grouped_workspace_bytes(const muon_group* groups, int n_groups);
 
 /*
- * zeropower_via_newtonschulz5 ([PG] 核心思想) on every matrix of a stack:
+ * The Newton-Schulz function ([PG] 核心思想) on every matrix of a stack:
  *   X = G / (||G||_F + eps)  (on G^T if rows > cols),
  *   `steps` times: A = X X^T;  B = b A + c A A;  X = a X + B X,
  *   out = X (transposed back), written as bf16 [batch, rows, cols].
@@ -107,8 +107,8 @@ muon_status muon_ns5(const void* G, int g_dtype, void* out_bf16,
 
 /*
  * One Muon step on a stack of same-shape weights ([MCS] 四, [PG] 核心思想/分布式细节):
- *   buf <- buf + (1 - momentum) (g - buf)                 (momentum_buffer.lerp_)
- *   u   <- g + momentum (buf - g)  if nesterov, else buf  (grad.lerp(buf, momentum))
+ *   buf <- buf + (1 - momentum) (g - buf)
+ *   u   <- g + momentum (buf - g)  if nesterov, else buf
  *   O   <- NS(u) as in muon_ns5 (kept in fp32 for the update)
  *   p   <- (1 - lr weight_decay) p - lr s O,   s = lr_scale > 0 ? lr_scale
  *                                                 : max(1, rows/cols)^0.5

@@ -7,7 +7,7 @@ the computation runs in the library's CUDA kernels.  There is no fallback:
 if the library is not built, or no sm_103a GPU is current, calls raise.
 
 Entry points mirror the C ABI:
-  ns5(G)                         zeropower_via_newtonschulz5 on a stack of matrices
+  ns5(G)                         the quintic Newton-Schulz iteration on a stack of matrices
   step(p, g, buf, ...)           one Muon step on a stack of same-shape weights
   step_grouped([(p, g, buf)...]) one Muon step on every group of a model
   adam_step([(p, g, m, v)...])   one DistAdam step on the non-matrix parameters
@@ -228,7 +228,7 @@ def _workspace(ws, need: int, device) -> Workspace:
 
 def ns5(G: torch.Tensor, out: torch.Tensor | None = None, steps: int = STEPS, coeffs=COEFFS,
         eps: float = EPS, workspace: Workspace | None = None, stream=None) -> torch.Tensor:
-    """zeropower_via_newtonschulz5 of every matrix of G ([b, r, c] or [r, c]); bf16 result."""
+    """The quintic Newton-Schulz iteration of every matrix of G ([b, r, c] or [r, c]); bf16 result."""
     L = load_library()
     squeeze = G.dim() == 2
     G3 = _as3d(G, "G")

@@ -1,12 +1,12 @@
 // prologue.cu -- the elementwise head of the Muon step, one pass over HBM:
 //
-//   buf <- buf + (1 - beta) (g - buf)        momentum_buffer.lerp_(grad, 1 - momentum)
-//   u   <- g + beta (buf - g)                grad.lerp(momentum_buffer, momentum)
+//   buf <- buf + (1 - beta) (g - buf)        momentum buffer moved towards g
+//   u   <- g + beta (buf - g)                Nesterov blend
 //                                            (or u = buf without Nesterov, u = g for NS only)
 //   X   <- bf16(u), or bf16(u^T) when rows > cols (padded leading dimension)
 //   partial sums of u^2 for the Frobenius norm, one per block
 //
-// ("Muon Custom Sizing 实战", section 四, second pass; the norm is the X.norm()
+// ("Muon Custom Sizing 实战", section 四, second pass; the norm is the Frobenius norm
 // of "parameter-golf train_gpt.py 源码精读", section 核心思想.)  The division by
 // ||u||_F + eps is folded into the first Gram and update epilogues, which sum
 // the partials in a fixed order, so the result is deterministic.

@@ -9,26 +9,26 @@ what the pages describe.  The pages cited below are:
 
 * [PG] "parameter-golf train_gpt.py 源码精读：Muon 优化器、Int8 量化与 DDP
   数据加载全解", part 1 "Muon 优化器是如何工作的":
-  - section "核心思想：把矩阵梯度'正交化'" prints ``zeropower_via_newtonschulz5``:
-    cast to bf16, divide by ``X.norm()`` (Frobenius), then ``steps`` times
-    ``A = X X^T; B = b A + c A A; X = a X + B X``;
+  - section "核心思想：把矩阵梯度'正交化'" gives the Newton-Schulz function:
+    cast to bf16, divide by the Frobenius norm, then ``steps`` rounds of
+    A = X X^T; B = b A + c A A; X = a X + B X;
   - section "分布式细节：每个 rank 只算 1/N 的参数" gives the shape rescale
-    ``g *= max(1, m/n) ** 0.5``.
+    factor max(1, m/n)^(1/2) on the NS result.
 * [MCS] "Muon Custom Sizing 实战：modded-nanogpt 将注意力与 MLP 参数合并进同一
   reduce_scatter 调用，把 124M GPT 训练压进 150 秒":
   - section 2.3 gives ``(a, b, c) = (3.4445, -4.7750, 2.0315)``, five rounds;
-  - section 四 ("第二遍") gives the momentum pair
-    ``momentum_buffer.lerp_(grad, 1 - momentum)`` then
-    ``update_grad = grad.lerp(momentum_buffer, momentum)``, the decoupled
-    decay ``eff_weight_decay = lr * wd`` applied to the parameter copy, and the
-    write-back of the NS result with ``alpha = -eff_lr``.
+  - section 四 (second pass) gives the momentum pair: the buffer moves towards
+    the gradient by 1 - momentum, then the gradient moves towards the updated
+    buffer by momentum (Nesterov); the decoupled decay by the factor
+    1 - lr * wd on the parameter; and the NS result added with weight
+    -lr * rescale.
 
 Readings taken where the pages are silent or loose (each is listed in the
 design notes with its reason):
 
-* eps: the printed loop divides by ``X.norm()`` alone; here the divisor is
+* eps: the page's loop divides by the norm alone; here the divisor is
   ``||X||_F + eps`` so that a zero update gives X = 0 instead of NaN.
-* norm kind: [MCS] says "spectral norm", [PG]'s code takes ``X.norm()``, the
+* norm kind: [MCS] speaks of the spectral norm, [PG]'s code takes the
   Frobenius norm.  The code wins: Frobenius.
 * orientation: when rows > cols the iteration runs on the transpose and the
   result is transposed back (the Gram matrix is then the smaller m x m one).
@@ -61,7 +61,7 @@ def _f64(x) -> np.ndarray:
 
 
 def momentum_buffer_update(buf, grad, momentum: float) -> np.ndarray:
-    """buf.lerp_(grad, 1 - momentum), i.e. buf + (1 - momentum) * (grad - buf).
+    """buf + (1 - momentum) * (grad - buf): the buffer moved towards the gradient.
 
     [MCS] section 四, second pass: the momentum buffer is lerped towards the
     gradient by weight ``1 - momentum`` before the Nesterov blend.
@@ -72,10 +72,10 @@ def momentum_buffer_update(buf, grad, momentum: float) -> np.ndarray:
 
 
 def nesterov_blend(grad, buf, momentum: float) -> np.ndarray:
-    """grad.lerp(buf, momentum), i.e. grad + momentum * (buf - grad).
+    """grad + momentum * (buf - grad): the Nesterov blend.
 
-    [MCS] section 四: ``update_grad = grad.lerp(momentum_buffer, momentum)``,
-    taken with the buffer already updated.
+    [MCS] section 四: the gradient moved towards the momentum buffer by
+    ``momentum``, taken with the buffer already updated.
     """
     grad = _f64(grad)
     buf = _f64(buf)
@@ -83,14 +83,14 @@ def nesterov_blend(grad, buf, momentum: float) -> np.ndarray:
 
 
 def frobenius_normalise(X, eps: float = NS5_EPS) -> np.ndarray:
-    """X / (||X||_F + eps).  [PG] section 核心思想: ``X /= X.norm()``."""
+    """X / (||X||_F + eps).  [PG] section 核心思想: one Frobenius normalisation."""
     X = _f64(X)
     return X / (np.sqrt(np.sum(X * X)) + eps)
 
 
 def newton_schulz5(G, steps: int = NS5_STEPS, coeffs=NS5_COEFFS,
                    eps: float = NS5_EPS) -> np.ndarray:
-    """zeropower_via_newtonschulz5 on one 2-D matrix, in float64.
+    """The quintic Newton-Schulz iteration on one 2-D matrix, in float64.
 
     [PG] section 核心思想: normalise once, then ``steps`` rounds of
     A = X X^T;  B = b A + c (A A);  X = a X + B X.
@@ -115,7 +115,7 @@ def newton_schulz5(G, steps: int = NS5_STEPS, coeffs=NS5_COEFFS,
 
 
 def rescale_factor(rows: int, cols: int) -> float:
-    """max(1, rows/cols) ** 0.5.  [PG] section 分布式细节: ``g *= max(1, m/n) ** 0.5``."""
+    """max(1, rows/cols) ** 0.5.  [PG] section 分布式细节: the shape rescale of the NS result."""
     return max(1.0, rows / cols) ** 0.5
 
 
@@ -123,8 +123,8 @@ def apply_update(param, O, lr: float, weight_decay: float,
                  lr_scale: float) -> np.ndarray:
     """p * (1 - lr * wd) - lr * lr_scale * O.
 
-    [MCS] section 四: decay ``lr * wd`` on the parameter copy, then the NS
-    result is added with ``alpha = -eff_lr`` where eff_lr = lr * rescale.
+    [MCS] section 四: decay by lr * wd on the parameter, then the NS result
+    added with weight -lr * rescale.
     """
     p = _f64(param)
     return (1.0 - lr * weight_decay) * p - (lr * lr_scale) * _f64(O)
