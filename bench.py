@@ -334,13 +334,14 @@ def run_gpu(args, wl):
     h2d = sum(t.numel() * t.element_size() for t in host_g)
     d2h = sum(t.numel() * t.element_size() for t in host_p)
     e2e_steps = max(1, min(args.steps, 20))
-    # Three streams and two device gradient buffers.  Step k's gradient upload
-    # (copy stream in) goes into buffer k % 2 once step k-2 is done with it, so it
-    # runs beside step k-1; step k runs on the main stream once its upload is in;
-    # its parameters are then snapshotted on the device (once the snapshot of
-    # step k-1 has been read back) and read back to the host from the snapshot
-    # (copy stream out) while step k+1 computes.  Every copy of every step is
-    # inside the timed region.
+    # Three streams, two device gradient buffers and two device parameter
+    # snapshots.  Step k's gradient upload (copy stream in) goes into buffer
+    # k % 2 once step k-2 is done with it, so it runs beside step k-1; step k
+    # runs on the main stream once its upload is in; its parameters are then
+    # copied on the device into snapshot k % 2 (once the read-back of step k-2
+    # from that snapshot is done) and read back to the host from it (copy stream
+    # out) while step k+1 computes, so the read-back stream never waits for a
+    # snapshot.  Every copy of every step is inside the timed region.
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     grads2 = [G.clone() for _, G, _ in tensors]
     step2 = muon.GroupedStep([(P, G2, B) for (P, _, B), G2 in zip(tensors, grads2)],
@@ -348,7 +349,7 @@ def run_gpu(args, wl):
                              nesterov=wl.nesterov, steps=wl.steps)
     dev_g = [[G for _, G, _ in tensors], grads2]
     steps_ab = [step, step2]
-    snap = [torch.empty_like(P) for P, _, _ in tensors]
+    snap = [[torch.empty_like(P) for P, _, _ in tensors] for _ in range(2)]
     ev_in = [torch.cuda.Event() for _ in range(e2e_steps)]
     ev_done = [torch.cuda.Event() for _ in range(e2e_steps)]
     ev_out = [torch.cuda.Event() for _ in range(e2e_steps)]
@@ -364,14 +365,14 @@ def run_gpu(args, wl):
             ev_in[k].record(up)
         stream.wait_event(ev_in[k])
         steps_ab[k % 2]()
-        if k > 0:
-            stream.wait_event(ev_out[k - 1])
-        for (P, _, _), sp in zip(tensors, snap):
+        if k > 1:
+            stream.wait_event(ev_out[k - 2])
+        for (P, _, _), sp in zip(tensors, snap[k % 2]):
             sp.copy_(P, non_blocking=True)
         ev_done[k].record(stream)
         down.wait_event(ev_done[k])
         with torch.cuda.stream(down):
-            for sp, hp in zip(snap, host_p):
+            for sp, hp in zip(snap[k % 2], host_p):
                 hp.copy_(sp, non_blocking=True)
             ev_out[k].record(down)
     stream.wait_event(ev_out[e2e_steps - 1])
@@ -384,9 +385,9 @@ def run_gpu(args, wl):
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "ms_per_step": e2e_ms / e2e_steps,
            "schedule": "gradient upload (copy stream, two device gradient buffers) and "
-                       "parameter read-back from a device snapshot (second copy stream) of "
-                       "neighbouring steps overlap the compute; every copy of every step "
-                       "inside the timed region"}
+                       "parameter read-back from device snapshots (second copy stream, two "
+                       "snapshots) of neighbouring steps overlap the compute; every copy of "
+                       "every step inside the timed region"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
