@@ -132,6 +132,14 @@ __device__ __forceinline__ bool b_mn_major(const TileCtx& T, int kb) {
   return STAGE == kStageGram ? T.x0_u != 0 : b_transposed<STAGE>(T.tn, kb);
 }
 
+// A diagonal tile of a symmetric stage (Gram X X^T, Poly A A): each CTA's half
+// of operand B is the same 128 rows, in the same layout, as its operand A, so
+// only A is loaded and the MMAs read it for B too.
+template <int STAGE>
+__device__ __forceinline__ bool b_is_a(const TileCtx& T) {
+  return STAGE != kStageUpdate && T.pr == T.tn;
+}
+
 __device__ __forceinline__ void record_failure(unsigned int* status, volatile int* abort_flag,
                                                unsigned int bit) {
   *abort_flag = 1;
@@ -155,6 +163,7 @@ __device__ bool produce_tile(const TileCtx& T, uint8_t* smem, uint64_t* full, ui
                              int rank) {
   using C = Cfg;
   const int tm = 2 * T.pr + rank;  // this CTA's 128-row block
+  const bool b_from_a = b_is_a<STAGE>(T);
   for (int kb = 0; kb < T.k_blocks; ++kb) {
     // the pair's MMAs (issued by the even CTA) are done with this slot
     if (!ptx::mbar_wait(&empty[ps.stage], ps.phase ^ 1u, abort_flag)) return false;
@@ -162,7 +171,9 @@ __device__ bool produce_tile(const TileCtx& T, uint8_t* smem, uint64_t* full, ui
     uint8_t* sb = sa + C::kABytes;
     // both CTAs' copies complete on the even CTA's barrier for this slot
     const uint32_t bar = leader_full0 + ps.stage * 8;
-    if (rank == 0) ptx::mbar_arrive_expect_tx(&full[ps.stage], 2 * C::kStageBytes);
+    if (rank == 0)
+      ptx::mbar_arrive_expect_tx(&full[ps.stage],
+                                 2 * (b_from_a ? C::kABytes : C::kStageBytes));
     // operand A: this CTA's 128 rows x 64 k-columns, or (below the stored
     // tiles) the 64 x 128 block at the transposed position, MN-major
     if (a_mn_major<STAGE>(T, kb)) {
@@ -173,7 +184,9 @@ __device__ bool produce_tile(const TileCtx& T, uint8_t* smem, uint64_t* full, ui
     } else {
       ptx::tma_load_3d_pair(sa, T.a, kb * kTileK, tm * kTileM, T.mat, bar);
     }
-    if (b_mn_major<STAGE>(T, kb)) {
+    if (b_from_a) {
+      // (the MMAs read operand B from operand A's slot)
+    } else if (b_mn_major<STAGE>(T, kb)) {
       // operand B = X[k][j] (update), or the transposed block (Poly below the
       // stored tiles, a first-round Gram of u), MN-major: this CTA's 128
       // columns as 2 slabs of 64 columns x 64 k-rows
@@ -229,9 +242,10 @@ __device__ bool mma_tile(const TileCtx& T, uint8_t* smem, uint64_t* full, uint64
     // fence is needed here)
     if (!ptx::mbar_wait(&full[ms.stage], ms.phase, abort_flag)) return false;
     const uint32_t sa = ptx::smem_u32(smem + ms.stage * C::kStageBytes);
-    const uint32_t sb = sa + C::kABytes;
+    const bool b_from_a = b_is_a<STAGE>(T);
+    const uint32_t sb = b_from_a ? sa : sa + C::kABytes;
     const bool a_mn = a_mn_major<STAGE>(T, kb);
-    const bool b_mn = b_mn_major<STAGE>(T, kb);
+    const bool b_mn = b_from_a ? a_mn : b_mn_major<STAGE>(T, kb);
     const uint32_t idesc = ptx::idesc_bf16(2 * kTileM, C::kBN, b_mn, a_mn);
 #pragma unroll
     for (int k = 0; k < kTileK / 16; ++k) {
