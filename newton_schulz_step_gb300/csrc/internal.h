@@ -262,7 +262,7 @@ cudaError_t launch_prologue(const PrologueLaunch& l, int mode, bool pdl, cudaStr
 cudaError_t launch_small(const SmallLaunch& l, int total_blocks, int max_mn, cudaStream_t s);
 cudaError_t launch_apply(const ApplyLaunch& l, bool to_param, cudaStream_t s);
 // The streamed parameter write (ApplyLaunch streamed fields), a programmatic
-// dependent of the persistent rounds kernel, `blocks` CTAs of 256 threads.
+// dependent of the last update launch, `blocks` CTAs of 256 threads.
 cudaError_t launch_apply_stream(const ApplyLaunch& l, int blocks, cudaStream_t s);
 constexpr unsigned int kRoundsSignalsPerTile = 8;  // completion-counter adds per stored pair tile
 // One launch of a GEMM stage over `pair_tiles` cluster tiles (two 128 x 256

@@ -32,11 +32,11 @@ std::atomic<int> g_fused_enabled{1};
 // NS rounds of tensor-core groups: 0 one launch per stage and round, 1 one
 // persistent launch per chunk, 2 (default) persistent when a round is short
 std::atomic<int> g_rounds_enabled{2};
-// 1: the parameter write streams beside the persistent rounds kernel when one
-// such launch covers every tensor-core matrix of the call (apply_stream_kernel)
+// 1: the parameter write streams beside the last update (apply_stream_kernel)
+// when one staged chunk covers every tensor-core matrix of the call
 std::atomic<int> g_stream_apply_enabled{1};
-// ... and only while the whole rounds launch is estimated under this (the
-// streamed write's waits give up after 2 s)
+// ... and only while what it waits beside (the whole rounds launch, or one
+// round) is estimated under this (the streamed write's waits give up after 2 s)
 constexpr double kStreamMaxUs = 1e5;
 
 // The persistent launch pays off while stage boundaries (launch, pipeline fill,
@@ -180,7 +180,7 @@ struct GPlan {
   bool tall = false, small = false;
   int ldx = 0, lda = 0, nparts = 0;
   size_t x0 = 0, x1 = 0, am = 0, bm = 0, parts = 0, xs = 0;  // workspace offsets
-  int ctr = 0;  // first per-matrix completion counter (persistent rounds kernel)
+  int ctr = 0;  // first per-matrix completion counter (rounds kernel, streamed write)
 };
 
 constexpr size_t kStatusBytes = 256;
@@ -617,7 +617,7 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
     pl.total_blocks = blocks;
     const bool pdl = small_launched && c0 == 0;
     pl.wait_prior = pdl ? 1 : 0;
-    if (c0 == 0) {  // the persistent rounds kernel's completion counters start at zero
+    if (c0 == 0) {  // the per-matrix completion counters start at zero
       pl.zero = reinterpret_cast<unsigned int*>(ws + kStatusBytes);
       int n = 0;
       for (const GPlan* g : big) n += g->batch;
@@ -726,8 +726,9 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
     return sc.lr * scale;
   };
   if (stream) {
-    // -- apply, streamed: matrices in the order the rounds kernel finishes them
-    //    (ascending n, as build_rounds orders its problems)
+    // -- apply, streamed: matrices in the order the last update finishes them
+    //    (ascending n, as build_rounds orders its problems and build_gemm walks
+    //    the update stage)
     std::vector<GPlan*> order(big);
     std::stable_sort(order.begin(), order.end(),
                      [](GPlan* x, GPlan* y) { return x->n < y->n; });

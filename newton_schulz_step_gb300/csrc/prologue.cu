@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
   __shared__ float red[8];
   // the first Gram stage may be scheduled once every block here has started
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // completion counters of the persistent rounds kernel, which reads them only
+  // per-matrix completion counters of the GEMMs, which read them only
   // after this grid has completed
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < L.n_zero; i += blockDim.x) L.zero[i] = 0u;
@@ -305,22 +305,22 @@ __global__ void __launch_bounds__(256) apply_kernel(const __grid_constant__ Appl
 
 // ------------------------------------------------------------ streamed apply
 // The same parameter write, p <- (1 - lr wd) p - lr_eff O, launched as a
-// programmatic dependent of the persistent rounds kernel so that it runs
-// beside that kernel's last round: each block claims work units (a few rows
-// of one matrix, ~8192 elements) in the order the rounds kernel finishes
-// matrices, waits until the matrix's completion counter shows its last round
-// stored, and streams the rows.  O is already in the parameter's orientation
-// (the last round of a rows > cols matrix stores O^T), so every access is a
-// coalesced row access and the kernel needs almost no shared memory: one of
-// its blocks fits on an SM beside a rounds CTA.  Requires cols % 8 == 0
-// (16-byte row segments).
+// programmatic dependent of the last update (the persistent rounds kernel, or
+// the last round's update launch) so that it runs beside it: each block claims
+// work units (a few rows of one matrix, ~8192 elements) in the order that
+// update finishes matrices, waits until the matrix's completion counter shows
+// its last update stored, and streams the rows.  O is already in the
+// parameter's orientation (the last update of a rows > cols matrix stores
+// O^T), so every access is a coalesced row access and the kernel needs almost
+// no shared memory: one of its blocks fits on an SM beside a GEMM CTA.
+// Requires cols % 8 == 0 (16-byte row segments).
 constexpr int kStreamSeg = 8;    // elements per thread access (16 B of O, 32 B of p)
 constexpr int kStreamDepth = 2;  // row segments per thread in flight
 
 // Counter wait of the streamed apply: acquire, bounded, ended early by a set
 // status word.  One thread per block polls, with a backoff from 1 to 8 us:
-// the counters are the rounds kernel's own, which its epilogues update and
-// its scheduler warps poll, so these waits must not crowd their L2 lines.
+// the counters are the GEMM's own, which its epilogues update (and the rounds
+// kernel's scheduler warps poll), so these waits must not crowd their L2 lines.
 __device__ __forceinline__ bool wait_done(const unsigned int* p, unsigned int target,
                                           const unsigned int* status) {
   unsigned int v;
@@ -341,8 +341,8 @@ __device__ __forceinline__ bool wait_done(const unsigned int* p, unsigned int ta
   }
 }
 
-// (at most 64 registers: four blocks per SM once the rounds kernel has left,
-// one beside a rounds CTA; measured faster than deeper, fewer blocks)
+// (at most 64 registers: four blocks per SM once the GEMM CTAs have left,
+// one beside a GEMM CTA; measured faster than deeper, fewer blocks)
 __global__ void __launch_bounds__(256, 4) apply_stream_kernel(const __grid_constant__ ApplyLaunch L) {
   __shared__ int s_unit;
   // thread 0 claims the block's next unit while the block works on the current one
@@ -363,8 +363,8 @@ __global__ void __launch_bounds__(256, 4) apply_stream_kernel(const __grid_const
       }
       s_unit = u;
     }
-    // (thread 0's acquire of the counter and this barrier order the rounds
-    // kernel's stores of O before every thread's loads of it)
+    // (thread 0's acquire of the counter and this barrier order the last
+    // update's stores of O before every thread's loads of it)
     __syncthreads();
     const int u = s_unit;
     __syncthreads();  // s_unit is rewritten by the next claim only after every thread read it
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(256, 4) apply_stream_kernel(const __grid_const
       }
     }
   }
-  // Programmatic dependent of the rounds kernel: the grid completes only after
+  // Programmatic dependent of the last update: the grid completes only after
   // it (and so after everything before it in the stream)
   if (blockIdx.x == 0 && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
