@@ -18,7 +18,10 @@
  *     as (hdim, 4*dim) is passed as batch 4 of (hdim, dim): the same bytes.
  *   - Every data pointer is device memory owned by the caller, 16-byte
  *     aligned.  Parameters and momentum buffers are updated in place;
- *     gradients are only read.  The library allocates no device memory.
+ *     gradients are only read.  No call allocates device memory; the one
+ *     device memory the library itself holds is the fixed 64 MiB scratch of
+ *     muon_step_noalloc(), a static array that every GPU which loads the
+ *     library keeps until the process exits.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
  *     work is enqueued on it asynchronously; no entry point synchronises
  *     except muon_workspace_status().
@@ -27,6 +30,14 @@
  *     aligned, and zero-filled before its first use (it carries a sticky
  *     device error word).  Calls that share a workspace must not overlap on
  *     the GPU.
+ *   - Failure (no counterpart on the pages): every device-side wait is
+ *     bounded (2 s).  A wait that gives up sets the workspace's error word;
+ *     from then on the waits of the other kernels still running end within
+ *     microseconds, and every kernel of every later call on that workspace
+ *     returns at entry, so those calls change nothing (parameters, momentum
+ *     and outputs keep their values) until muon_workspace_status() clears
+ *     the word.  The call during which the wait gave up may have written part
+ *     of its results.
  *   - Argument errors are reported before anything is enqueued.  A CUDA error
  *     while enqueuing gives MUON_ERR_CUDA.  No C++ exception crosses the ABI.
  *   - NS runs in bf16 on the tensor cores (fp32 accumulation and epilogues)
@@ -132,12 +143,25 @@ muon_status muon_step(float* params, const void* grads, int g_dtype, float* mome
  * exceeds 64 MiB returns MUON_ERR_WORKSPACE.  The first call on a device looks
  * up the array's device address, so make it before any stream capture.  All
  * calls on a device share the array: calls that overlap on the GPU race.
+ * Each call clears the array's sticky error word on `stream` after its
+ * argument checks and before its first kernel, so the word reports the latest
+ * call on the device: read it with muon_noalloc_status().
  */
 muon_status muon_step_noalloc(float* params, const void* grads, int g_dtype, float* momentum_buf,
                               int batch, int rows, int cols,
                               float momentum, int nesterov, float lr, float weight_decay,
                               float lr_scale, int steps, float a, float b, float c, float eps,
                               void* stream);
+
+/*
+ * muon_workspace_status() for the built-in scratch of muon_step_noalloc() on
+ * the current device (no counterpart on the pages): synchronises `stream`,
+ * then returns MUON_OK, or MUON_ERR_TIMEOUT if a bounded device-side wait
+ * gave up during the latest muon_step_noalloc() call on this device (or
+ * during a muon_selftest_wait_timeout() on the scratch since).  clear != 0
+ * resets the word afterwards.
+ */
+muon_status muon_noalloc_status(void* stream, int clear);
 
 /*
  * muon_step on every group of a model at once (the pages stack the weights of
@@ -165,7 +189,9 @@ muon_status muon_workspace_status(const void* workspace, size_t workspace_bytes,
  * with, is on a barrier that nothing completes; after `limit_us` (1..100000)
  * it gives up and records the timeout in the workspace's status word, as a
  * stalled GEMM would.  muon_workspace_status() then reports MUON_ERR_TIMEOUT.
- * Nothing faults, hangs or is left pending on the GPU.
+ * workspace = NULL targets the built-in scratch of muon_step_noalloc() on the
+ * current device instead (workspace_bytes is then ignored), read back with
+ * muon_noalloc_status().  Nothing faults, hangs or is left pending on the GPU.
  */
 muon_status muon_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int limit_us,
                                        void* stream);

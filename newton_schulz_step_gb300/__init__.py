@@ -24,7 +24,8 @@ __all__ = [
     "COEFFS", "EPS", "MuonError", "load_library", "library_path", "workspace_bytes",
     "grouped_workspace_bytes", "Workspace", "ns5", "step", "step_noalloc", "step_grouped",
     "GroupedStep", "AdamStep", "adam_step", "ADAM_LR", "ADAM_BETAS", "ADAM_EPS",
-    "workspace_status", "status_string", "kernel_launch_count", "trace_begin", "trace_end",
+    "workspace_status", "noalloc_status", "selftest_wait_timeout", "status_string",
+    "kernel_launch_count", "trace_begin", "trace_end",
     "set_fused_ns", "fused_ns", "set_persistent_rounds", "persistent_rounds",
     "set_streamed_apply", "streamed_apply", "KERNEL_KINDS",
 ]
@@ -104,6 +105,8 @@ def load_library():
     L.muon_step_grouped.restype = ci
     L.muon_workspace_status.argtypes = [vp, sz, vp, ci]
     L.muon_workspace_status.restype = ci
+    L.muon_noalloc_status.argtypes = [vp, ci]
+    L.muon_noalloc_status.restype = ci
     L.muon_selftest_wait_timeout.argtypes = [vp, sz, ci, vp]
     L.muon_selftest_wait_timeout.restype = ci
     L.muon_adam_step.argtypes = [ctypes.POINTER(_AdamTensor), ci, ci, cf, cf, cf, cf, cf, vp]
@@ -268,18 +271,24 @@ def step_noalloc(params, grads, momentum_buf, *, momentum: float, lr: float,
                  weight_decay: float, nesterov: bool = True, lr_scale: float = 0.0,
                  steps: int = STEPS, coeffs=COEFFS, eps: float = EPS, stream=None):
     """step() without a workspace, for callers that may not allocate device memory:
-    the library's built-in 64 MiB device scratch is used instead."""
+    the library's built-in 64 MiB device scratch (of the tensors' GPU) is used
+    instead.  The call runs with the tensors' device current, so the scratch and
+    the kernels are on that device."""
     L = load_library()
     p3, g3, m3 = _as3d(params, "params"), _as3d(grads, "grads"), _as3d(momentum_buf, "momentum_buf")
     if p3.dtype != torch.float32 or m3.dtype != torch.float32:
         raise TypeError("params and momentum_buf must be float32")
     if not (p3.shape == g3.shape == m3.shape):
         raise ValueError("params, grads and momentum_buf must have the same shape")
+    if not (p3.device == g3.device == m3.device):
+        raise ValueError("params, grads and momentum_buf must be on the same device")
     b, r, c = g3.shape
     a_, b_, c_ = coeffs
-    _raise(L.muon_step_noalloc(p3.data_ptr(), g3.data_ptr(), _gdt(g3), m3.data_ptr(), b, r, c,
-                               momentum, int(bool(nesterov)), lr, weight_decay, lr_scale, steps,
-                               a_, b_, c_, eps, _stream_handle(stream)), "muon_step_noalloc")
+    with torch.cuda.device(p3.device):
+        _raise(L.muon_step_noalloc(p3.data_ptr(), g3.data_ptr(), _gdt(g3), m3.data_ptr(), b, r, c,
+                                   momentum, int(bool(nesterov)), lr, weight_decay, lr_scale,
+                                   steps, a_, b_, c_, eps, _stream_handle(stream)),
+               "muon_step_noalloc")
 
 
 def _normalise_groups(groups):
@@ -387,9 +396,17 @@ def workspace_status(workspace: Workspace, clear: bool = False, stream=None) -> 
                                                     _stream_handle(stream), int(clear)))
 
 
-def selftest_wait_timeout(workspace: Workspace, limit_us: int = 1000, stream=None):
-    """Run the device-side bounded-wait timeout path once (see the C header)."""
-    _raise(load_library().muon_selftest_wait_timeout(workspace.ptr, workspace.nbytes, limit_us,
+def noalloc_status(clear: bool = False, stream=None) -> int:
+    """Synchronise and read the error word of step_noalloc()'s built-in scratch on the
+    current device (0 = ok, 4 = a bounded wait gave up during the latest call)."""
+    return int(load_library().muon_noalloc_status(_stream_handle(stream), int(clear)))
+
+
+def selftest_wait_timeout(workspace: Workspace | None, limit_us: int = 1000, stream=None):
+    """Run the device-side bounded-wait timeout path once (see the C header); with
+    workspace None it records the timeout in step_noalloc()'s built-in scratch."""
+    ptr, nbytes = (workspace.ptr, workspace.nbytes) if workspace is not None else (None, 0)
+    _raise(load_library().muon_selftest_wait_timeout(ptr, nbytes, limit_us,
                                                      _stream_handle(stream)),
            "muon_selftest_wait_timeout")
 

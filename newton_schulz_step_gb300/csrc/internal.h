@@ -61,6 +61,7 @@ struct PrologueLaunch {
   unsigned int* zero;     // counters the launch zeroes (block 0), or null
   int n_zero;
   unsigned int* zero_work;  // the streamed apply's claim counter, zeroed by block 0 (or null)
+  const unsigned int* status;  // sticky device error word: set at entry, the launch does nothing
 };
 
 // One tensor-core group of the grouped apply launch: the NS result O (bf16,
@@ -91,7 +92,8 @@ struct ApplyLaunch {
   // kernel: warps claim units in order from *work and wait for their matrix
   const unsigned int* done;
   unsigned int* work;
-  unsigned int* status;   // sticky device error word (a set word ends the waits)
+  unsigned int* status;   // sticky device error word: set at entry, the launch does
+                          // nothing; set later, it ends the streamed form's waits
   int total_units;
 };
 
@@ -115,6 +117,7 @@ struct SmallLaunch {
   int mode;               // PrologueMode
   int steps;
   float beta, a, b, c, eps, decay;
+  const unsigned int* status;  // sticky device error word: set at entry, the launch does nothing
 };
 
 struct GemmProblem {
@@ -279,5 +282,16 @@ cudaError_t launch_adam(const AdamLaunch& l, int blocks, cudaStream_t s);
 // after griddepcontrol.wait.
 cudaError_t launch_fused(const FusedLaunch& l, cudaStream_t s);
 int adam_blocks_per_sm();  // resident Adam blocks per SM on the current device (0 on error)
+
+// muon_step whose workspace's sticky error word is cleared on the stream after
+// the argument checks and before the first kernel (muon_api.cu).
+muon_status step_clearing_status(float* params, const void* grads, int g_dtype,
+                                 float* momentum_buf, int batch, int rows, int cols,
+                                 float momentum, int nesterov, float lr, float weight_decay,
+                                 float lr_scale, int steps, float a, float b, float c, float eps,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+// Device address and size of the built-in scratch of muon_step_noalloc on the
+// current device (noalloc.cu).
+muon_status noalloc_scratch(void** out, size_t* bytes);
 
 }  // namespace muon

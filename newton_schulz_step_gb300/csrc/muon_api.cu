@@ -469,8 +469,10 @@ muon_status build_rounds(RoundsLaunch& R, const std::vector<GPlan*>& chunk, cons
 }
 
 // ------------------------------------------------------------ the step
+// clear_status: zero the workspace's sticky error word on `st` once every
+// argument has been checked, before the first launch.
 muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
-                     size_t ws_bytes, cudaStream_t st) {
+                     size_t ws_bytes, cudaStream_t st, bool clear_status = false) {
   muon_status s = check_scalars(sc);
   if (s != MUON_OK) return s;
   for (const GPlan& g : gs) {
@@ -488,6 +490,8 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
   s = current_device(&sms);
   if (s != MUON_OK) return s;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (clear_status && cudaMemsetAsync(ws, 0, sizeof(unsigned int), st) != cudaSuccess)
+    return MUON_ERR_CUDA;
 
   // -- small matrices: one fp32 kernel for all of them, launched first; it lets
   //    the grouped prologue below start at once and run beside it
@@ -503,6 +507,7 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
     sl.c = sc.c;
     sl.eps = sc.eps;
     sl.decay = 1.0f - sc.lr * sc.wd;
+    sl.status = reinterpret_cast<const unsigned int*>(ws);
     int blocks = 0, max_mn = 0;
     auto flush = [&]() -> muon_status {
       if (sl.n_groups == 0) return MUON_OK;
@@ -591,6 +596,7 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
     PrologueLaunch pl;
     std::memset(&pl, 0, sizeof(pl));
     pl.beta = sc.beta;
+    pl.status = reinterpret_cast<const unsigned int*>(ws);
     double bytes = 0;
     int blocks = 0;
     for (size_t k = c0; k < std::min(big.size(), c0 + kMaxPrologueGroups); ++k) {
@@ -778,6 +784,7 @@ muon_status run_step(std::vector<GPlan>& gs, const Scalars& sc, void* workspace,
   for (size_t c0 = 0; c0 < big.size(); c0 += kMaxPrologueGroups) {
     ApplyLaunch al;
     std::memset(&al, 0, sizeof(al));
+    al.status = reinterpret_cast<unsigned int*>(ws);
     double bytes = 0;
     int blocks = 0;
     const size_t c1 = std::min(big.size(), c0 + kMaxPrologueGroups);
@@ -824,6 +831,26 @@ GPlan make_plan(float* p, const void* g, int gdt, float* buf, __nv_bfloat16* out
 }
 
 }  // namespace
+
+namespace muon {
+
+muon_status step_clearing_status(float* params, const void* grads, int g_dtype,
+                                 float* momentum_buf, int batch, int rows, int cols,
+                                 float momentum, int nesterov, float lr, float weight_decay,
+                                 float lr_scale, int steps, float a, float b, float c, float eps,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  try {
+    std::vector<GPlan> gs{make_plan(params, grads, g_dtype, momentum_buf, nullptr, batch, rows,
+                                    cols, lr_scale)};
+    const Scalars sc{nesterov ? kPrologueNesterov : kProloguePlain, momentum, lr, weight_decay,
+                     steps, a, b, c, eps};
+    return run_step(gs, sc, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), true);
+  } catch (...) {
+    return MUON_ERR_CUDA;
+  }
+}
+
+}  // namespace muon
 
 // ============================================================ C ABI
 extern "C" {
@@ -915,13 +942,18 @@ muon_status muon_workspace_status(const void* workspace, size_t workspace_bytes,
 
 muon_status muon_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int limit_us,
                                        void* stream) {
-  if (!workspace || workspace_bytes < kStatusBytes ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return MUON_ERR_WORKSPACE;
   if (limit_us < 1 || limit_us > 100000) return MUON_ERR_INVALID_ARG;
+  if (workspace && (workspace_bytes < kStatusBytes ||
+                    (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+    return MUON_ERR_WORKSPACE;
   int sms = 0;
-  const muon_status s = current_device(&sms);
+  muon_status s = current_device(&sms);
   if (s != MUON_OK) return s;
+  if (!workspace) {
+    // the built-in scratch of muon_step_noalloc on the current device
+    s = noalloc_scratch(&workspace, &workspace_bytes);
+    if (s != MUON_OK) return s;
+  }
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const cudaError_t e = launch_wait_selftest(static_cast<unsigned int*>(workspace),
                                              1000ull * static_cast<unsigned long long>(limit_us),

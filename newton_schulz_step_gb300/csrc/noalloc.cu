@@ -11,6 +11,11 @@
 // Every call then passes it to muon_step, which runs the usual kernels on it.
 // All calls on a device share the one array: calls that overlap on the GPU
 // (different streams, or different host threads) race on it.
+//
+// The array starts with the sticky device error word that every workspace
+// carries.  Each call clears that word on its stream (after its argument
+// checks, before its first kernel), so the word always describes the latest
+// call on the device; muon_noalloc_status reads it.
 #include <mutex>
 
 #include "internal.h"
@@ -27,8 +32,13 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[64] = {nullptr};
 
-// Device address of the scratch on the current device (looked up once).
-muon_status noalloc_scratch(void** out) {
+}  // namespace
+
+namespace muon {
+
+// Device address and size of the scratch on the current device (the address
+// is looked up once per device).
+muon_status noalloc_scratch(void** out, size_t* bytes) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MUON_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
@@ -38,10 +48,11 @@ muon_status noalloc_scratch(void** out) {
     g_noalloc_addr[dev] = p;
   }
   *out = g_noalloc_addr[dev];
+  *bytes = kNoAllocScratchBytes;
   return MUON_OK;
 }
 
-}  // namespace
+}  // namespace muon
 
 extern "C" muon_status muon_step_noalloc(float* params, const void* grads, int g_dtype,
                                          float* momentum_buf, int batch, int rows, int cols,
@@ -52,13 +63,22 @@ extern "C" muon_status muon_step_noalloc(float* params, const void* grads, int g
   if (need == 0) return MUON_ERR_INVALID_ARG;
   if (need > kNoAllocScratchBytes) return MUON_ERR_WORKSPACE;  // beyond the built-in scratch
   void* scratch = nullptr;
-  const muon_status s = noalloc_scratch(&scratch);
+  size_t bytes = 0;
+  const muon_status s = muon::noalloc_scratch(&scratch, &bytes);
   if (s != MUON_OK) return s;
-  // The scratch keeps the previous call's contents.  Nothing in it has to start
-  // at zero: every value a call reads was written earlier in the same call, and
-  // the device error word at its start is only ever OR-ed by a kernel whose
-  // bounded wait timed out (static device memory starts zeroed).
-  return muon_step(params, grads, g_dtype, momentum_buf, batch, rows, cols, momentum, nesterov,
-                   lr, weight_decay, lr_scale, steps, a, b, c, eps, scratch,
-                   kNoAllocScratchBytes, stream);
+  // The scratch keeps the previous call's contents.  Everything a call reads
+  // was written earlier in the same call, except the sticky error word at its
+  // start: a word left set by an earlier call would make every kernel of this
+  // one return at entry, so the step clears it first.
+  return muon::step_clearing_status(params, grads, g_dtype, momentum_buf, batch, rows, cols,
+                                    momentum, nesterov, lr, weight_decay, lr_scale, steps, a, b,
+                                    c, eps, scratch, bytes, stream);
+}
+
+extern "C" muon_status muon_noalloc_status(void* stream, int clear) {
+  void* scratch = nullptr;
+  size_t bytes = 0;
+  const muon_status s = muon::noalloc_scratch(&scratch, &bytes);
+  if (s != MUON_OK) return s;
+  return muon_workspace_status(scratch, bytes, stream, clear);
 }

@@ -89,7 +89,7 @@ __device__ __forceinline__ void fail(Ctx& x) {
 
 // All threads: wait for the commit of the MMAs with barrier phase `phase` (bounded).
 __device__ __forceinline__ void wait_mma(Ctx& x, uint64_t* bar, uint32_t& phase) {
-  if (!ptx::mbar_wait(bar, phase, x.bad)) fail(x);
+  if (!ptx::mbar_wait(bar, phase, x.bad, x.status)) fail(x);
   phase ^= 1u;
   ptx::tc_fence_after();
 }
@@ -174,9 +174,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
   // X0 and the norm partials are written by the prologue, the kernel before
   ptx::griddep_wait();
+  // A failure already recorded on this workspace: the CTA issues no copy and
+  // no MMA (every later wait returns at once), but still passes every barrier
+  // its pair partner passes.
+  if (x.tid == 0 && ptx::status_set(L.status)) *bad = 1;
+  __syncthreads();
   uint32_t ld_phase = 0, mma_phase = 0, mma2_phase = 0;
   constexpr int kStoreTid = 32;   // issues (and waits for) the X stores
-  if (x.tid == 0) {
+  if (x.tid == 0 && !*bad) {
     ptx::mbar_arrive_expect_tx(ld_bar, n_slab * kSlab);
     for (int q = 0; q < n_slab; ++q)
       ptx::tma_load_3d(X + q * kSlab, tm[0], 64 * q, row0, mat, ld_bar);
@@ -190,7 +195,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if ((x.tid & 31) == 0) *s_norm = 1.0f / (sqrtf(acc) + L.eps);
   }
-  if (!ptx::mbar_wait(ld_bar, ld_phase, x.bad)) fail(x);
+  if (!ptx::mbar_wait(ld_bar, ld_phase, x.bad, x.status)) fail(x);
   ld_phase ^= 1u;
   ptx::tc_fence_before();
   if constexpr (kPair) ptx::cluster_sync();   // both CTAs' X0 slabs have landed
@@ -294,7 +299,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
     if constexpr (kPair) {
       // the other CTA's X rows have landed in this CTA's slabs
-      if (x.tid == 0 && !*bad && !ptx::mbar_wait(ld_bar, ld_phase, x.bad)) fail(x);
+      if (x.tid == 0 && !*bad && !ptx::mbar_wait(ld_bar, ld_phase, x.bad, x.status)) fail(x);
       ld_phase ^= 1u;
     }
     epilogue_done<kPair>();

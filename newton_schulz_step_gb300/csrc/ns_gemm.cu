@@ -140,10 +140,21 @@ __device__ __forceinline__ bool b_is_a(const TileCtx& T) {
   return STAGE != kStageUpdate && T.pr == T.tn;
 }
 
-__device__ __forceinline__ void record_failure(unsigned int* status, volatile int* abort_flag,
-                                               unsigned int bit) {
-  *abort_flag = 1;
-  atomicOr(status, bit);
+// How a role gives up: the CTA's abort flag (ends every wait of the CTA's
+// other roles), the peer CTA's abort flag (shared::cluster address; ends the
+// pair's waits at once) and the launch's sticky status word in global memory
+// (ends, after a short delay, every wait of every other CTA, and makes later
+// kernels on this workspace return at entry).
+struct Abort {
+  volatile int* flag;
+  uint32_t peer_flag;
+  unsigned int* status;
+};
+
+__device__ __forceinline__ void record_failure(const Abort& ab, unsigned int bit) {
+  *ab.flag = 1;
+  ptx::st_cluster_u32(ab.peer_flag, 1u);
+  atomicOr(ab.status, bit);
 }
 
 __device__ __forceinline__ int first_tile() { return blockIdx.x >> 1; }
@@ -159,14 +170,13 @@ struct ProdState {
 // Issues the k-blocks of one tile into the ring.  False on a timed-out wait.
 template <int STAGE>
 __device__ bool produce_tile(const TileCtx& T, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                             uint32_t leader_full0, ProdState& ps, volatile int* abort_flag,
-                             int rank) {
+                             uint32_t leader_full0, ProdState& ps, const Abort& ab, int rank) {
   using C = Cfg;
   const int tm = 2 * T.pr + rank;  // this CTA's 128-row block
   const bool b_from_a = b_is_a<STAGE>(T);
   for (int kb = 0; kb < T.k_blocks; ++kb) {
     // the pair's MMAs (issued by the even CTA) are done with this slot
-    if (!ptx::mbar_wait(&empty[ps.stage], ps.phase ^ 1u, abort_flag)) return false;
+    if (!ptx::mbar_wait(&empty[ps.stage], ps.phase ^ 1u, ab.flag, ab.status)) return false;
     uint8_t* sa = smem + ps.stage * C::kStageBytes;
     uint8_t* sb = sa + C::kABytes;
     // both CTAs' copies complete on the even CTA's barrier for this slot
@@ -211,12 +221,11 @@ __device__ bool produce_tile(const TileCtx& T, uint8_t* smem, uint64_t* full, ui
 
 // Before exit: the pair's MMAs have released every armed stage, so its copies
 // landed and no commit arrival can still be on its way to this CTA.
-__device__ void drain_producer(const ProdState& ps, uint64_t* empty, unsigned int* status,
-                               volatile int* abort_flag) {
+__device__ void drain_producer(const ProdState& ps, uint64_t* empty, const Abort& ab) {
   for (int s = 0; s < Cfg::kStages; ++s)
     if (ps.armed & (1u << s))
       if (!ptx::mbar_wait(&empty[s], (ps.armed_parity >> s) & 1u, nullptr))
-        record_failure(status, abort_flag, kErrTimeoutDrain);
+        record_failure(ab, kErrTimeoutDrain);
 }
 
 // ------------------------------------------------------------ MMA issuer
@@ -231,16 +240,16 @@ struct MmaState {
 template <int STAGE>
 __device__ bool mma_tile(const TileCtx& T, uint8_t* smem, uint64_t* full, uint64_t* empty,
                          uint64_t* acc_full, uint64_t* acc_empty, uint32_t tmem_base,
-                         MmaState& ms, volatile int* abort_flag) {
+                         MmaState& ms, const Abort& ab) {
   using C = Cfg;
   // both CTAs' epilogues have drained this accumulator
-  if (!ptx::mbar_wait(&acc_empty[ms.acc], ms.acc_phase ^ 1u, abort_flag)) return false;
+  if (!ptx::mbar_wait(&acc_empty[ms.acc], ms.acc_phase ^ 1u, ab.flag, ab.status)) return false;
   ptx::tc_fence_after();
   const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ms.acc * C::kBN);
   for (int kb = 0; kb < T.k_blocks; ++kb) {
     // (the barrier orders the TMA writes before these MMA reads; no tcgen05
     // fence is needed here)
-    if (!ptx::mbar_wait(&full[ms.stage], ms.phase, abort_flag)) return false;
+    if (!ptx::mbar_wait(&full[ms.stage], ms.phase, ab.flag, ab.status)) return false;
     const uint32_t sa = ptx::smem_u32(smem + ms.stage * C::kStageBytes);
     const bool b_from_a = b_is_a<STAGE>(T);
     const uint32_t sb = b_from_a ? sa : sa + C::kABytes;
@@ -274,9 +283,9 @@ __device__ bool mma_tile(const TileCtx& T, uint8_t* smem, uint64_t* full, uint64
 }
 
 // Every MMA issued by this thread completes before TMEM is released.
-__device__ void drain_mma(uint64_t* drain, unsigned int* status, volatile int* abort_flag) {
+__device__ void drain_mma(uint64_t* drain, const Abort& ab) {
   ptx::mma_commit_pair(drain, 1);
-  if (!ptx::mbar_wait(drain, 0, nullptr)) record_failure(status, abort_flag, kErrTimeoutDrain);
+  if (!ptx::mbar_wait(drain, 0, nullptr)) record_failure(ab, kErrTimeoutDrain);
 }
 
 // ------------------------------------------------------------ epilogue helpers
@@ -337,7 +346,7 @@ struct EpiState {
 template <int STAGE>
 __device__ bool epilogue_tile(const TileCtx& T, const GemmScalars& k, uint64_t* acc_full,
                               uint64_t* acc_empty, uint64_t* my_in, uint8_t* my_slots,
-                              uint32_t tmem_base, EpiState& es, volatile int* abort_flag,
+                              uint32_t tmem_base, EpiState& es, const Abort& ab,
                               int quarter, int lane, int rank, const unsigned int* dep,
                               unsigned int dep_target) {
   using C = Cfg;
@@ -360,7 +369,7 @@ __device__ bool epilogue_tile(const TileCtx& T, const GemmScalars& k, uint64_t* 
     int ok = 1;
     if (lane == 0 && u_hi > 0) {
       if (dep != nullptr) {
-        if (!ptx::wait_counter(dep, dep_target, abort_flag)) ok = 0;
+        if (!ptx::wait_counter(dep, dep_target, ab.flag, ab.status)) ok = 0;
         ptx::fence_proxy_async_global();
       }
       if (ok) {
@@ -377,7 +386,7 @@ __device__ bool epilogue_tile(const TileCtx& T, const GemmScalars& k, uint64_t* 
     if (__shfl_sync(0xffffffffu, ok, 0) == 0) return false;
   }
 
-  const bool got = ptx::mbar_wait(&acc_full[es.acc], es.acc_phase, abort_flag);
+  const bool got = ptx::mbar_wait(&acc_full[es.acc], es.acc_phase, ab.flag, ab.status);
   __syncwarp();
   if (!got) return false;
   ptx::tc_fence_after();
@@ -390,7 +399,7 @@ __device__ bool epilogue_tile(const TileCtx& T, const GemmScalars& k, uint64_t* 
     uint8_t* blk = my_slots + es.slot * C::kSlotBytes;
     if constexpr (kPoly) {
       const uint32_t par = (es.in_par >> es.slot) & 1u;
-      if (!ptx::mbar_wait(&my_in[es.slot], par, abort_flag)) failed = true;
+      if (!ptx::mbar_wait(&my_in[es.slot], par, ab.flag, ab.status)) failed = true;
       es.in_par ^= 1u << es.slot;
     } else {
       // the slot's previous bulk store (two units ago) has read its data
@@ -545,6 +554,31 @@ __device__ __forceinline__ uint32_t setup_cta(const Smem& m, int warp) {
   return *m.tmem_slot;
 }
 
+// The pair's abort context (after setup_cta).
+__device__ __forceinline__ Abort pair_abort(const Smem& m, unsigned int* status, int rank) {
+  Abort ab;
+  ab.flag = m.abort_flag;
+  ab.peer_flag = ptx::mapa_shared(ptx::smem_u32((const void*)m.abort_flag),
+                                  static_cast<uint32_t>(rank ^ 1));
+  ab.status = status;
+  return ab;
+}
+
+// Called by every thread of both CTAs once the previous grid's output is
+// visible (after griddep_wait): true if the status word already records a
+// failure (an earlier kernel on this workspace gave up, or a CTA of this
+// launch did), in which case the pair does no work at all.  Both CTAs read the
+// word and raise both flags, and the cluster barrier makes the decision common
+// to the pair, so neither CTA runs roles that wait on roles the other skips.
+__device__ __forceinline__ bool skip_at_entry(const Abort& ab) {
+  if (threadIdx.x == 0 && ptx::status_set(ab.status)) {
+    *ab.flag = 1;
+    ptx::st_cluster_u32(ab.peer_flag, 1u);
+  }
+  ptx::cluster_sync();
+  return *ab.flag != 0;
+}
+
 __device__ __forceinline__ void teardown_cta(uint32_t tmem_base, int warp) {
   __syncwarp();
   ptx::tc_fence_before();
@@ -634,8 +668,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   const uint32_t tmem_base = setup_cta(sm, warp);
   // setup above overlapped the previous stage's tail; its output is read below
   ptx::griddep_wait();
+  const Abort ab = pair_abort(sm, L.status, rank);
+  const bool skip = skip_at_entry(ab);
 
-  if (warp == 0) {
+  if (skip) {
+    // an earlier failure on this workspace: nothing is read or written
+  } else if (warp == 0) {
     if (lane == 0) {
       for (int p = 0; p < L.n_prob; ++p) {
         ptx::prefetch_tmap(&L.tm_a[p]);
@@ -647,13 +685,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const uint32_t leader_full0 = ptx::mapa_shared(ptx::smem_u32(sm.full), 0);
       for (int t = first_tile(); t < L.total_tiles; t += tile_stride()) {
         const TileCtx T = staged_ctx(L, decode_tile<STAGE>(L, t));
-        if (!produce_tile<STAGE>(T, sm.ring, sm.full, sm.empty, leader_full0, ps,
-                                 sm.abort_flag, rank)) {
-          record_failure(L.status, sm.abort_flag, kErrTimeoutProducer);
+        if (!produce_tile<STAGE>(T, sm.ring, sm.full, sm.empty, leader_full0, ps, ab, rank)) {
+          record_failure(ab, kErrTimeoutProducer);
           break;
         }
       }
-      drain_producer(ps, sm.empty, L.status, sm.abort_flag);
+      drain_producer(ps, sm.empty, ab);
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
@@ -661,12 +698,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       for (int t = first_tile(); t < L.total_tiles; t += tile_stride()) {
         const TileCtx T = staged_ctx(L, decode_tile<STAGE>(L, t));
         if (!mma_tile<STAGE>(T, sm.ring, sm.full, sm.empty, sm.acc_full, sm.acc_empty, tmem_base,
-                             ms, sm.abort_flag)) {
-          record_failure(L.status, sm.abort_flag, kErrTimeoutMma);
+                             ms, ab)) {
+          record_failure(ab, kErrTimeoutMma);
           break;
         }
       }
-      drain_mma(sm.drain, L.status, sm.abort_flag);
+      drain_mma(sm.drain, ab);
     }
   } else {
     const int quarter = warp & 3;
@@ -678,8 +715,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const Tile tl = decode_tile<STAGE>(L, t);
       const TileCtx T = staged_ctx(L, tl);
       if (!epilogue_tile<STAGE>(T, k, sm.acc_full, sm.acc_empty, my_in, my_slots, tmem_base, es,
-                                sm.abort_flag, quarter, lane, rank, nullptr, 0u)) {
-        record_failure(L.status, sm.abort_flag, kErrTimeoutEpilogue);
+                                ab, quarter, lane, rank, nullptr, 0u)) {
+        record_failure(ab, kErrTimeoutEpilogue);
         break;
       }
       // last update before a streamed parameter write: this warp's blocks of
@@ -822,8 +859,13 @@ __global__ void __launch_bounds__(Cfg::kRoundsThreads, 1)
   // may start once every CTA of this grid is resident, and after the prologue
   // has completed (it zeroes the apply's claim counter)
   ptx::griddep_launch_dependents();
+  const Abort ab = pair_abort(sm, L.status, rank);
+  const bool skip = skip_at_entry(ab);
 
-  if (warp == 0) {
+  if (skip) {
+    // an earlier failure on this workspace: nothing is read or written (the
+    // streamed write, waiting on this kernel's counters, sees the same word)
+  } else if (warp == 0) {
     if (lane == 0) {
       for (int p = 0; p < L.n_prob; ++p) {
         ptx::prefetch_tmap(&L.x_op[p][0]);
@@ -841,8 +883,8 @@ __global__ void __launch_bounds__(Cfg::kRoundsThreads, 1)
       for (int i = first_tile(); i < L.total_items; i += tile_stride(), ++n) {
         const int q = n % Cfg::kQueue;
         if (!ptx::mbar_wait(&sm.q_full[q], static_cast<uint32_t>((n / Cfg::kQueue) & 1),
-                            sm.abort_flag)) {
-          record_failure(L.status, sm.abort_flag, kErrTimeoutProducer);
+                            ab.flag, ab.status)) {
+          record_failure(ab, kErrTimeoutProducer);
           break;
         }
         const int4 e = queue[q];
@@ -861,20 +903,17 @@ __global__ void __launch_bounds__(Cfg::kRoundsThreads, 1)
         const TileCtx T = rounds_ctx(L, it);
         bool ok;
         if (it.s == kStageGram)
-          ok = produce_tile<kStageGram>(T, sm.ring, sm.full, sm.empty, leader_full0, ps,
-                                        sm.abort_flag, rank);
+          ok = produce_tile<kStageGram>(T, sm.ring, sm.full, sm.empty, leader_full0, ps, ab, rank);
         else if (it.s == kStagePoly)
-          ok = produce_tile<kStagePoly>(T, sm.ring, sm.full, sm.empty, leader_full0, ps,
-                                        sm.abort_flag, rank);
+          ok = produce_tile<kStagePoly>(T, sm.ring, sm.full, sm.empty, leader_full0, ps, ab, rank);
         else
-          ok = produce_tile<kStageUpdate>(T, sm.ring, sm.full, sm.empty, leader_full0, ps,
-                                          sm.abort_flag, rank);
+          ok = produce_tile<kStageUpdate>(T, sm.ring, sm.full, sm.empty, leader_full0, ps, ab, rank);
         if (!ok) {
-          record_failure(L.status, sm.abort_flag, kErrTimeoutProducer);
+          record_failure(ab, kErrTimeoutProducer);
           break;
         }
       }
-      drain_producer(ps, sm.empty, L.status, sm.abort_flag);
+      drain_producer(ps, sm.empty, ab);
     }
   } else if (warp == 2 + Cfg::kEpiWarps) {
     // scheduler: the tiles in order, each once the stages before it (of its
@@ -884,15 +923,15 @@ __global__ void __launch_bounds__(Cfg::kRoundsThreads, 1)
       for (int i = first_tile(); i < L.total_items; i += tile_stride(), ++n) {
         const int q = n % Cfg::kQueue;
         if (!ptx::mbar_wait(&sm.q_empty[q], static_cast<uint32_t>(((n / Cfg::kQueue) & 1) ^ 1),
-                            sm.abort_flag)) {
-          record_failure(L.status, sm.abort_flag, kErrTimeoutProducer);
+                            ab.flag, ab.status)) {
+          record_failure(ab, kErrTimeoutProducer);
           break;
         }
         const Item it = decode_item(L, i);
         const unsigned int target = dep_target(L, it);
-        if (target > 0 &&
-            !ptx::wait_counter(L.done + L.prob[it.p].done_begin + it.mat, target, sm.abort_flag)) {
-          record_failure(L.status, sm.abort_flag, kErrTimeoutDepend);
+        if (target > 0 && !ptx::wait_counter(L.done + L.prob[it.p].done_begin + it.mat, target,
+                                             ab.flag, ab.status)) {
+          record_failure(ab, kErrTimeoutDepend);
           break;
         }
         queue[q] = make_int4(it.r | (it.s << 8) | (it.p << 12), it.mat, it.pr, it.tn);
@@ -908,19 +947,19 @@ __global__ void __launch_bounds__(Cfg::kRoundsThreads, 1)
         bool ok;
         if (it.s == kStageGram)
           ok = mma_tile<kStageGram>(T, sm.ring, sm.full, sm.empty, sm.acc_full, sm.acc_empty,
-                                    tmem_base, ms, sm.abort_flag);
+                                    tmem_base, ms, ab);
         else if (it.s == kStagePoly)
           ok = mma_tile<kStagePoly>(T, sm.ring, sm.full, sm.empty, sm.acc_full, sm.acc_empty,
-                                    tmem_base, ms, sm.abort_flag);
+                                    tmem_base, ms, ab);
         else
           ok = mma_tile<kStageUpdate>(T, sm.ring, sm.full, sm.empty, sm.acc_full, sm.acc_empty,
-                                      tmem_base, ms, sm.abort_flag);
+                                      tmem_base, ms, ab);
         if (!ok) {
-          record_failure(L.status, sm.abort_flag, kErrTimeoutMma);
+          record_failure(ab, kErrTimeoutMma);
           break;
         }
       }
-      drain_mma(sm.drain, L.status, sm.abort_flag);
+      drain_mma(sm.drain, ab);
     }
   } else {
     const int quarter = warp & 3;
@@ -935,18 +974,18 @@ __global__ void __launch_bounds__(Cfg::kRoundsThreads, 1)
       bool ok;
       if (it.s == kStageGram)
         ok = epilogue_tile<kStageGram>(T, k, sm.acc_full, sm.acc_empty, my_in, my_slots,
-                                       tmem_base, es, sm.abort_flag, quarter, lane, rank,
+                                       tmem_base, es, ab, quarter, lane, rank,
                                        nullptr, 0u);
       else if (it.s == kStagePoly)
         ok = epilogue_tile<kStagePoly>(T, k, sm.acc_full, sm.acc_empty, my_in, my_slots,
-                                       tmem_base, es, sm.abort_flag, quarter, lane, rank, ctr,
+                                       tmem_base, es, ab, quarter, lane, rank, ctr,
                                        dep_target(L, it));
       else
         ok = epilogue_tile<kStageUpdate>(T, k, sm.acc_full, sm.acc_empty, my_in, my_slots,
-                                         tmem_base, es, sm.abort_flag, quarter, lane, rank,
+                                         tmem_base, es, ab, quarter, lane, rank,
                                          nullptr, 0u);
       if (!ok) {
-        record_failure(L.status, sm.abort_flag, kErrTimeoutEpilogue);
+        record_failure(ab, kErrTimeoutEpilogue);
         break;
       }
       // this warp's blocks of the tile are in global memory: count them
@@ -975,7 +1014,7 @@ __global__ void wait_selftest_kernel(unsigned int* status, unsigned long long li
   ptx::mbar_init(&bar, 1);
   abort_flag = 0;
   ptx::fence_mbar_init();
-  if (!ptx::mbar_wait(&bar, 0, &abort_flag, limit_ns)) atomicOr(status, kErrTimeoutEpilogue);
+  if (!ptx::mbar_wait(&bar, 0, &abort_flag, nullptr, limit_ns)) atomicOr(status, kErrTimeoutEpilogue);
   // complete the barrier's phase so nothing is left pending
   ptx::mbar_arrive(&bar);
 }

@@ -65,6 +65,8 @@ __global__ void __launch_bounds__(kSmallThreads) small_ns_kernel(
 
   // the next grid (independent work) may start right away
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // a failure already recorded on this workspace: this call changes nothing
+  if (*reinterpret_cast<const volatile unsigned int*>(L.status) != 0u) return;
 
   int gi = 0;
   while (gi + 1 < L.n_groups && static_cast<int>(blockIdx.x) >= L.grp[gi + 1].block_begin) ++gi;

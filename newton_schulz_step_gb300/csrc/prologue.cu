@@ -101,6 +101,12 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
   __shared__ float red[8];
   // the first Gram stage may be scheduled once every block here has started
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // a failure already recorded on this workspace: this call changes nothing
+  // (block 0 still keeps the completion chain, below)
+  if (*reinterpret_cast<const volatile unsigned int*>(L.status) != 0u) {
+    if (L.wait_prior && blockIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+    return;
+  }
   // per-matrix completion counters of the GEMMs, which read them only
   // after this grid has completed
   if (blockIdx.x == 0) {
@@ -221,6 +227,9 @@ __global__ void __launch_bounds__(256) apply_kernel(const __grid_constant__ Appl
   __shared__ float stage_tile[64][65];
   // launched as a programmatic dependent of the last update: its output is O
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // a failure recorded on this workspace (by this call's NS or an earlier
+  // call): O is not valid, nothing is written
+  if (*reinterpret_cast<const volatile unsigned int*>(L.status) != 0u) return;
   int gi = 0;
   while (gi + 1 < L.n_groups && static_cast<int>(blockIdx.x) >= L.grp[gi + 1].block_begin) ++gi;
   const ApplyGroup& A = L.grp[gi];
@@ -345,9 +354,13 @@ __device__ __forceinline__ bool wait_done(const unsigned int* p, unsigned int ta
 // one beside a GEMM CTA; measured faster than deeper, fewer blocks)
 __global__ void __launch_bounds__(256, 4) apply_stream_kernel(const __grid_constant__ ApplyLaunch L) {
   __shared__ int s_unit;
-  // thread 0 claims the block's next unit while the block works on the current one
+  // thread 0 claims the block's next unit while the block works on the current
+  // one; with a failure already recorded on this workspace it claims nothing
   unsigned int next = 0;
-  if (threadIdx.x == 0) next = atomicAdd(L.work, 1u);
+  if (threadIdx.x == 0)
+    next = *reinterpret_cast<const volatile unsigned int*>(L.status) != 0u
+               ? static_cast<unsigned int>(L.total_units)
+               : atomicAdd(L.work, 1u);
   while (true) {
     if (threadIdx.x == 0) {
       int u = static_cast<int>(next);

@@ -2,9 +2,10 @@
 // tcgen05 (TMEM allocation, MMA, commit, loads) and bounded waits.
 //
 // Every wait here is bounded: after kWaitTimeoutNs of %globaltimer without
-// progress (or once another role has raised the CTA's abort flag) it returns
-// false, and the caller records the timeout and unwinds.  No wait spins
-// forever.
+// progress, once another role has raised the CTA's abort flag, or (for waits
+// given the workspace's status word) once any kernel has recorded a failure
+// there, it returns false, and the caller records the timeout and unwinds.
+// No wait spins forever.
 #pragma once
 
 #include <cuda.h>
@@ -16,6 +17,15 @@ namespace ptx {
 // A wait that has not completed after this long gives up (normal waits take
 // microseconds; the longest kernel of a step takes tens of milliseconds).
 constexpr uint64_t kWaitTimeoutNs = 2000ull * 1000ull * 1000ull;
+// A wait that has lasted this long also polls the sticky status word in global
+// memory, so that a failure anywhere ends it within microseconds instead of
+// after its own timeout; shorter waits (every wait of a healthy kernel) never
+// touch that word.
+constexpr uint64_t kStatusPollNs = 20ull * 1000ull;
+
+__device__ __forceinline__ bool status_set(const unsigned int* status) {
+  return status != nullptr && *reinterpret_cast<const volatile unsigned int*>(status) != 0u;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -66,9 +76,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Returns false on
-// timeout or when *abort_flag becomes non-zero (abort_flag may be null).
+// timeout, when *abort_flag becomes non-zero, or (after kStatusPollNs) when
+// the status word is set; abort_flag and status may be null.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           const volatile int* abort_flag,
+                                          const unsigned int* status = nullptr,
                                           uint64_t timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
@@ -77,7 +89,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     if (mbar_try_wait(bar, parity)) return true;
     if ((++spins & 63u) == 0u) {
       if (abort_flag != nullptr && *abort_flag) return false;
-      if (globaltimer() - t0 > timeout_ns) return false;
+      const uint64_t dt = globaltimer() - t0;
+      if (dt > timeout_ns) return false;
+      if (dt > kStatusPollNs && status_set(status)) return false;
     }
   }
 }
@@ -91,10 +105,12 @@ __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
 __device__ __forceinline__ void red_release_gpu_add(unsigned int* p, unsigned int v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-// Wait until *p >= target (acquire).  Returns false on timeout or when
-// *abort_flag becomes non-zero (abort_flag may be null).
+// Wait until *p >= target (acquire).  Returns false on timeout, when
+// *abort_flag becomes non-zero, or (after kStatusPollNs) when the status word
+// is set; abort_flag and status may be null.
 __device__ __forceinline__ bool wait_counter(const unsigned int* p, unsigned int target,
                                              const volatile int* abort_flag,
+                                             const unsigned int* status = nullptr,
                                              uint64_t timeout_ns = kWaitTimeoutNs) {
   if (ld_acquire_gpu(p) >= target) return true;
   const uint64_t t0 = globaltimer();
@@ -102,7 +118,9 @@ __device__ __forceinline__ bool wait_counter(const unsigned int* p, unsigned int
     __nanosleep(64);
     if (ld_acquire_gpu(p) >= target) return true;
     if (abort_flag != nullptr && *abort_flag) return false;
-    if (globaltimer() - t0 > timeout_ns) return false;
+    const uint64_t dt = globaltimer() - t0;
+    if (dt > timeout_ns) return false;
+    if (dt > kStatusPollNs && status_set(status)) return false;
   }
 }
 
@@ -119,20 +137,6 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-
-// The same box written to the same shared-memory offset of every CTA in
-// `cta_mask` (within the cluster); each destination CTA's barrier at `bar`'s
-// offset receives the transaction bytes.
-__device__ __forceinline__ void tma_load_3d_multicast(void* smem_dst, const CUtensorMap* map,
-                                                      int x, int y, int z, uint64_t* bar,
-                                                      uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z),
-      "h"(cta_mask)
       : "memory");
 }
 
@@ -162,19 +166,6 @@ __device__ __forceinline__ void bulk_wait() {
 // Order this thread's generic shared-memory writes before later async-proxy reads.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Hint: bring one box of a tiled tensor into L2 (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-
-// Hint: bring the 128-byte line holding `p` into L2.
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // Programmatic dependent launch: let the next grid in the stream be scheduled
@@ -214,6 +205,12 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
+}
+// 32-bit store into shared memory given by its shared::cluster address
+// (possibly another CTA's), e.g. to raise the peer CTA's abort flag.
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.relaxed.cluster.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(v)
+               : "memory");
 }
 // Arrive on a barrier given by its shared::cluster address (possibly another CTA's).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
@@ -269,16 +266,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-
-// Arrive once on the barrier at `bar`'s offset in every CTA of `cta_mask`
-// when every tcgen05 op issued so far by this thread is done.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 
@@ -365,42 +352,11 @@ __device__ __forceinline__ void tmem_ld32x2_sync(uint32_t t0, uint32_t t1, uint3
       : "r"(t0), "r"(t1)
       : "memory");
 }
-// The store counterpart (32 lanes x 32 columns from 32 registers per thread),
-// followed by the wait that makes the columns visible to later TMEM accesses.
-__device__ __forceinline__ void tmem_st32_sync(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
-      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
-      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
-      "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
-
-// 16-byte store into another CTA's shared memory (address from mapa_shared).
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x),
-               "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
 // Order global-memory accesses of the generic proxy (and those observed through
 // it) with this thread's later async-proxy (TMA) accesses, and vice versa.
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
-// Order this thread's generic writes to shared memory of any CTA of the
-// cluster before later async-proxy (tensor core) reads of it.
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-}
-
 // ------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor (tcgen05 form): start >> 4 in bits 0-13,
 // leading byte offset >> 4 in 16-29, stride byte offset >> 4 in 32-45,

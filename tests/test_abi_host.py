@@ -125,9 +125,19 @@ def test_ns5_argument_errors(lib):
 
 
 def test_selftest_argument_errors(lib):
-    assert lib.muon_selftest_wait_timeout(None, 1024, 1000, None) == WORKSPACE
+    assert lib.muon_selftest_wait_timeout(0x10010, 1024, 1000, None) == WORKSPACE
+    assert lib.muon_selftest_wait_timeout(0x10000, 16, 1000, None) == WORKSPACE
     assert lib.muon_selftest_wait_timeout(0x10000, 1024, 0, None) == INVALID
     assert lib.muon_selftest_wait_timeout(0x10000, 1024, 200000, None) == INVALID
+    assert lib.muon_selftest_wait_timeout(None, 0, 0, None) == INVALID
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU refusal")
+def test_noalloc_scratch_calls_without_gpu_are_refused(lib):
+    # NULL workspace = the built-in scratch of muon_step_noalloc: without a device
+    # there is no scratch, and nothing is launched
+    assert lib.muon_selftest_wait_timeout(None, 0, 1000, None) in (UNSUPPORTED, CUDA)
+    assert lib.muon_noalloc_status(None, 0) in (UNSUPPORTED, CUDA)
 
 
 def test_workspace_status_argument_errors(lib):
