@@ -144,45 +144,66 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle timing
-def oracle_sample(wl, per_group=1):
-    """A bounded sample of the workload for the CPU oracle: the first `per_group`
-    matrices of every group, drawn with the workload's CPU seeds."""
+# A workload whose counted NS flops per step stay under this is timed whole on the
+# host (the GPT-2 124M step is ~1.4 TFLOP, a few seconds on 16 cores); a larger
+# one is timed on one stored matrix per group and the time multiplied by the
+# group's stored count ("extrapolated").
+ORACLE_FULL_MAX_FLOPS = 2.0e12
+ORACLE_REPEATS = 3
+
+
+def _oracle_group_inputs(wl, gi, stored, device="cpu"):
+    """(params, grads, bufs) as float64 numpy [k, rows, cols] for the first `stored`
+    stored matrices of group gi (k = stored x the blocks each one is viewed as)."""
     import workloads
-    sample = []
-    for gi, grp in enumerate(wl.groups):
-        n_stored = grp.stored_shape[0]
-        per_stored = grp.batch // n_stored
-        for j in range(min(per_group, n_stored)):
-            p, g, b = workloads.draw_stored_matrix(wl, gi, j, "cpu")
-            shape = (per_stored, grp.rows, grp.cols)
-            sample.append((grp, p.reshape(shape), g.reshape(shape), b.reshape(shape)))
-    return sample
-
-
-def time_oracle(wl, per_group=1, repeats=1):
-    """Times the CPU float64 oracle on oracle_sample(); returns (seconds, counted flops)."""
+    grp = wl.groups[gi]
+    per_stored = grp.batch // grp.stored_shape[0]
+    ps, gs, bs = [], [], []
+    for j in range(stored):
+        p, g, b = workloads.draw_stored_matrix(wl, gi, j, device)
+        shape = (per_stored, grp.rows, grp.cols)
+        ps.append(p.reshape(shape).double().numpy())
+        gs.append(g.float().reshape(shape).double().numpy())
+        bs.append(b.reshape(shape).double().numpy())
     import numpy as np
+    return np.concatenate(ps), np.concatenate(gs), np.concatenate(bs)
+
+
+def oracle_plan(wl):
+    """'full' or 'extrapolated' for this workload's CPU oracle timing."""
+    return "full" if counted_ns_flops(wl.groups, wl.steps) <= ORACLE_FULL_MAX_FLOPS \
+        else "extrapolated"
+
+
+def time_oracle_step(wl, repeats=ORACLE_REPEATS):
+    """Seconds per Muon step of the CPU float64 oracle on the workload.
+
+    'full': every matrix of the step, the median of `repeats` timed steps on the
+    same inputs.  'extrapolated': one stored matrix per group, timed once, times the
+    group's stored count.  Returns (seconds, description)."""
     import oracle
-    import workloads  # noqa: F401
-    sample = oracle_sample(wl, per_group)
-    mats = [(grp, p.double().numpy(), g.float().double().numpy(), b.double().numpy())
-            for grp, p, g, b in sample]
-    flops = 0.0
-    for grp, p, _, _ in mats:
-        m, n = min(grp.rows, grp.cols), max(grp.rows, grp.cols)
-        flops += p.shape[0] * wl.steps * (4.0 * m * m * n + 2.0 * m ** 3)
-    best = float("inf")
-    for _ in range(repeats):
+    kw = dict(momentum=wl.momentum, nesterov=wl.nesterov, lr=wl.lr,
+              weight_decay=wl.weight_decay, steps=wl.steps)
+    if oracle_plan(wl) == "full":
+        inputs = [_oracle_group_inputs(wl, gi, grp.stored_shape[0])
+                  for gi, grp in enumerate(wl.groups)]
+        times = []
+        for _ in range(repeats):
+            t0 = time.perf_counter()
+            for p, g, b in inputs:
+                oracle.muon_step_batched(p, g, b, **kw)
+            times.append(time.perf_counter() - t0)
+        return statistics.median(times), (f"whole step ({wl.n_matrices} matrices), median of "
+                                          f"{repeats} timed steps")
+    total = 0.0
+    for gi, grp in enumerate(wl.groups):
+        p, g, b = _oracle_group_inputs(wl, gi, 1)
         t0 = time.perf_counter()
-        for grp, p, g, b in mats:
-            oracle.muon_step_batched(p, g, b, momentum=wl.momentum, nesterov=wl.nesterov,
-                                     lr=wl.lr, weight_decay=wl.weight_decay, steps=wl.steps)
-        best = min(best, time.perf_counter() - t0)
-    del np
-    return best, flops
-
-
-CPU_BASELINE_SECONDS = 10.0
+        oracle.muon_step_batched(p, g, b, **kw)
+        total += (time.perf_counter() - t0) * grp.stored_shape[0]
+    return total, ("extrapolated: one stored matrix per group ("
+                   + ", ".join(f"{g.rows}x{g.cols} x{g.stored_shape[0]}" for g in wl.groups)
+                   + ") timed once, times the group's count")
 
 
 def cpu_cores():
@@ -190,33 +211,44 @@ def cpu_cores():
     return int(n) if n and n.isdigit() else (os.cpu_count() or 1)
 
 
-def sample_text(wl, per_group):
-    return (f"first {per_group} stored matrix of each of the {len(wl.groups)} groups "
-            f"({', '.join(f'{g.rows}x{g.cols}' for g in wl.groups)}), full NS5 in float64")
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
 
 
 # ---------------------------------------------------------------- reference arm
 def run_reference(args, wl):
+    """The CPU float64 oracle timed on the host cores, on the same workload and metric:
+    each step is one whole oracle step ('full' workloads) or the extrapolated
+    one-matrix-per-group sample."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    per_group = 1
+    flops = counted_ns_flops(wl.groups, wl.steps)
     for _ in range(args.warmup):
-        time_oracle(wl, per_group)
-    times, flops = [], 0.0
+        time_oracle_step(wl, repeats=1)
+    times, how = [], ""
     for _ in range(args.steps):
-        t, flops = time_oracle(wl, per_group)
+        t, how = time_oracle_step(wl, repeats=1)
         times.append(t)
     total = sum(times)
     value = flops * len(times) / total / 1e12
+    sample = f"{how}; {args.steps} steps"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / len(times), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "sample": sample_text(wl, per_group)},
+        "config": {"workload": wl.name, "oracle": oracle_plan(wl), "sample": sample},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(),
-                         "kind": "oracle", "sample": sample_text(wl, per_group)},
+                         "cpu": cpu_model(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -225,20 +257,20 @@ def run_reference(args, wl):
 
 
 # ---------------------------------------------------------------- GPU arm
-def run_gpu(args, wl):
+NS_KINDS = ("gram", "poly", "update", "small_ns", "fused_ns", "rounds")
+# timed steps of the other workloads in the `configs` object (the headline
+# workload takes --steps): the d=4096 step is ~0.33 s
+CONFIG_STEPS = {"single-128x256": 50, "gpt-9L-d512": 50, "gpt2-124M-d768": 20,
+                "gpt-24L-d2048": 5, "gpt-32L-d4096": 3}
+
+
+def time_workload(muon, wl, dev, steps, warmup, use_graph, peaks, local, world):
+    """One workload on this GPU: the step timed with CUDA events (replayed as a CUDA
+    graph), then a traced pass of the same steps for per-kernel times.  Returns
+    (result dict, (tensors, step)) -- the tensors stay alive for the caller."""
     import torch
 
-    import newton_schulz_step_gb300 as muon
     import workloads
-
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    peaks = load_peaks()
-
     groups = workloads.make_workload(wl, dev)
     tensors = [(P, G, B) for _, P, G, B in groups]
     step = muon.GroupedStep(tensors, momentum=wl.momentum, lr=wl.lr,
@@ -248,7 +280,7 @@ def run_gpu(args, wl):
 
     run = step
     graph = None
-    if args.graph:
+    if use_graph:
         # capture the whole step (all launches) once; replay it every step
         for _ in range(2):
             step()
@@ -259,7 +291,7 @@ def run_gpu(args, wl):
         run = graph.replay
 
     lps = launches_per_step(step)
-    for _ in range(max(args.warmup, 0)):
+    for _ in range(max(warmup, 0)):
         run()
     torch.cuda.synchronize()
 
@@ -278,14 +310,14 @@ def run_gpu(args, wl):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if flush is None:
         e0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             run()
         e1.record(stream)
         torch.cuda.synchronize()
         local_ms = e0.elapsed_time(e1)
     else:
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
+               for _ in range(steps)]
         for a, b in evs:
             flush.fill_(1)
             a.record(stream)
@@ -295,14 +327,16 @@ def run_gpu(args, wl):
         local_ms = sum(a.elapsed_time(b) for a, b in evs)
     barrier(world)
     # graph replays launch the captured kernels without passing through the host counter
-    launches = lps * args.steps if graph is not None else muon.kernel_launch_count() - n0
+    launches = lps * steps if graph is not None else muon.kernel_launch_count() - n0
     clock = clocks.stop()
-    ms, units = aggregate_over_ranks(local_ms, flops * args.steps, world)
+    ms, units = aggregate_over_ranks(local_ms, flops * steps, world)
     value = units / (ms / 1e3) / 1e12
+    flushed = flush is not None
+    del flush
 
     # per-kernel times from a traced pass over the same steps (eager launches)
     muon.trace_begin(100000)
-    for _ in range(args.steps):
+    for _ in range(steps):
         step()
     recs = muon.trace_end(100000)
     torch.cuda.synchronize()
@@ -313,9 +347,9 @@ def run_gpu(args, wl):
         k["n"] += 1
         k["flops"] += r["flops"]
         k["bytes"] += r["bytes"]
-    ns_kinds = ("gram", "poly", "update", "small_ns", "fused_ns", "rounds")
-    ns_ms = sum(kinds[k]["ms"] for k in ns_kinds if k in kinds) / args.steps
-    traced_ms = sum(k["ms"] for k in kinds.values()) / args.steps
+    ns_ms = sum(kinds[k]["ms"] for k in NS_KINDS if k in kinds) / steps
+    ns_flops_exec = sum(kinds[k]["flops"] for k in NS_KINDS if k in kinds) / steps
+    traced_ms = sum(k["ms"] for k in kinds.values()) / steps
     dom_name, dom = max(kinds.items(), key=lambda kv: kv[1]["ms"])
     per_launch_ms = dom["ms"] / dom["n"]
     if dom["flops"] > 0:
@@ -339,19 +373,50 @@ def run_gpu(args, wl):
         ew_ms = sum(k["ms"] for k in ew)
         gbs = ew_bytes / (ew_ms / 1e3) / 1e9
         elementwise = {"gbs": gbs, "frac": gbs / peaks["hbm_gbs"],
-                       "ms_per_step": ew_ms / args.steps,
+                       "ms_per_step": ew_ms / steps,
                        "per_kernel": {name: {"gbs": kinds[name]["bytes"] / (kinds[name]["ms"] / 1e3) / 1e9,
-                                             "ms_per_step": kinds[name]["ms"] / args.steps}
+                                             "ms_per_step": kinds[name]["ms"] / steps}
                                       for name in ("prologue", "apply") if name in kinds}}
+    per_step_ms = ms / steps
+    res = {
+        "workload": wl.name, "steps": steps, "warmup": warmup, "ms_per_step": per_step_ms,
+        "us_per_step": 1e3 * per_step_ms, "tflops": value,
+        "frac_of_peak": value / peaks["bf16_tflops"],
+        "frac_of_sustained_peak": value / peaks["bf16_tflops_sustained"],
+        # the flops the kernels execute (Gram and Poly on the upper tiles only)
+        "method_tflops": ns_flops_exec / (per_step_ms / 1e3) / 1e12,
+        "counted_gflop_per_step": flops / 1e9,
+        "executed_gflop_per_step": ns_flops_exec / 1e9,
+        "matrices": wl.n_matrices,
+        "groups": [f"{g.batch}x{g.rows}x{g.cols}" for g in wl.groups],
+        "graph": bool(use_graph),
+        "l2": ("inputs larger than L2: %.0f MB of grads, params and momentum moved per step"
+               % (wl.n_elements * (2 + 8 + 8) / 1e6)) if not flushed else
+              ("L2 flushed before every timed step (%.0f MB written outside the step's "
+               "events); inputs %.1f MB" % (2 * l2_bytes / 1e6, in_bytes / 1e6)),
+        "ns_chain": {"ms_per_step": ns_ms, "tflops": flops / (ns_ms / 1e3) / 1e12,
+                     "frac": flops / (ns_ms / 1e3) / 1e12 / peaks["bf16_tflops"]},
+        "traced_ms_per_step": traced_ms,
+        "kernels": {k: {"ms_per_step": v["ms"] / steps, "launches_per_step": v["n"] / steps}
+                    for k, v in kinds.items()},
+        "elementwise": elementwise, "roofline": roof, "gpu_launches": launches, "clocks": clock,
+    }
+    return res, (tensors, step)
 
-    adam = time_adam(args, wl, dev, peaks) if wl.adam else None
 
-    # end to end through the public API with host buffers: grads in, params out
+def time_e2e(muon, wl, tensors, step, world):
+    """The same grouped step end to end through the public binding with host buffers:
+    every step's gradients uploaded from pinned host memory and its parameters read
+    back, inside the timed region."""
+    import torch
+    dev = tensors[0][0].device
+    stream = torch.cuda.current_stream()
+    flops = counted_ns_flops(wl.groups, wl.steps)
     host_g = [G.cpu().pin_memory() for _, G, _ in tensors]
     host_p = [torch.empty(P.shape, dtype=P.dtype, pin_memory=True) for P, _, _ in tensors]
     h2d = sum(t.numel() * t.element_size() for t in host_g)
     d2h = sum(t.numel() * t.element_size() for t in host_p)
-    e2e_steps = max(1, min(args.steps, 20))
+    e2e_steps = 20
     # Three streams, two device gradient buffers and two device parameter
     # snapshots.  Step k's gradient upload (copy stream in) goes into buffer
     # k % 2 once step k-2 is done with it, so it runs beside step k-1; step k
@@ -371,6 +436,7 @@ def run_gpu(args, wl):
     ev_in = [torch.cuda.Event() for _ in range(e2e_steps)]
     ev_done = [torch.cuda.Event() for _ in range(e2e_steps)]
     ev_out = [torch.cuda.Event() for _ in range(e2e_steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
@@ -399,51 +465,87 @@ def run_gpu(args, wl):
     barrier(world)
     e2e_ms = max(e0.elapsed_time(e1), 1e3 * (time.perf_counter() - t0))
     e2e_ms, e2e_units = aggregate_over_ranks(e2e_ms, flops * e2e_steps, world)
-    e2e = {"value": e2e_units / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "ms_per_step": e2e_ms / e2e_steps,
-           "schedule": "gradient upload (copy stream, two device gradient buffers) and "
-                       "parameter read-back from device snapshots (second copy stream, two "
-                       "snapshots) of neighbouring steps overlap the compute; every copy of "
-                       "every step inside the timed region"}
+    return {"value": e2e_units / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
+            "schedule": "gradient upload (copy stream, two device gradient buffers) and "
+                        "parameter read-back from device snapshots (second copy stream, two "
+                        "snapshots) of neighbouring steps overlap the compute; every copy of "
+                        "every step inside the timed region"}
 
+
+def run_gpu(args, wl):
+    import torch
+
+    import newton_schulz_step_gb300 as muon
+    import workloads
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+
+    head, (tensors, step) = time_workload(muon, wl, dev, args.steps, args.warmup,
+                                          bool(args.graph), peaks, local, world)
+    adam = time_adam(args, wl, dev, peaks) if wl.adam else None
+    e2e = time_e2e(muon, wl, tensors, step, world)
+    del tensors, step
+    torch.cuda.empty_cache()
+
+    do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # the sample, repeated until about 10 s of CPU work have been timed
-        secs, cflops, reps = 0.0, 0.0, 0
-        while reps == 0 or secs < CPU_BASELINE_SECONDS:
-            t, f = time_oracle(wl, 1)
-            secs, cflops, reps = secs + t, cflops + f, reps + 1
-        cpu = {"value": cflops / secs / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
-               "kind": "oracle", "sample": f"{sample_text(wl, 1)}, {reps} times",
-               "seconds": secs}
+    if do_cpu:
+        secs, how = time_oracle_step(wl)
+        flops = counted_ns_flops(wl.groups, wl.steps)
+        cpu = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
+               "cpu": cpu_model(), "kind": "oracle", "sample": how,
+               "ms_per_step": 1e3 * secs, "oracle": oracle_plan(wl)}
+
+    # every workload of the build, on the same GPU, one after the other
+    configs = {}
+    if not args.headline_only:
+        for name in workloads.WORKLOADS:
+            if name == wl.name:
+                res = dict(head)
+            else:
+                w = workloads.get(name)
+                res, keep = time_workload(muon, w, dev, min(args.steps, CONFIG_STEPS[name]),
+                                          args.warmup, bool(args.graph), peaks, local, world)
+                del keep
+                torch.cuda.empty_cache()
+            if do_cpu:
+                w = workloads.get(name)
+                if name == wl.name:
+                    secs, how = cpu["ms_per_step"] / 1e3, cpu["sample"]
+                else:
+                    secs, how = time_oracle_step(w)
+                res["oracle"] = {"ms_per_step": 1e3 * secs, "plan": oracle_plan(w),
+                                 "sample": how, "cores": cpu_cores(),
+                                 "speedup": 1e3 * secs / res["ms_per_step"]}
+            configs[name] = res
 
     if rank == 0:
-        per_step_ms = ms / args.steps
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step_ms,
-            "us_per_step": 1e3 * per_step_ms, "frac_of_peak": value / peaks["bf16_tflops"],
-            "frac_of_sustained_peak": value / peaks["bf16_tflops_sustained"],
+            "metric": METRIC, "value": head["tflops"], "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+            "us_per_step": head["us_per_step"], "frac_of_peak": head["frac_of_peak"],
+            "frac_of_sustained_peak": head["frac_of_sustained_peak"],
+            "method_tflops": head["method_tflops"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": wl.name, "matrices": wl.n_matrices,
-                       "groups": [f"{g.batch}x{g.rows}x{g.cols}" for g in wl.groups],
-                       "counted_gflop_per_step": flops / 1e9, "graph": bool(args.graph),
-                       "l2": ("inputs larger than L2: %.0f MB of grads, params and momentum "
-                              "moved per step" % (wl.n_elements * (2 + 8 + 8) / 1e6))
-                       if flush is None else
-                       ("L2 flushed before every timed step (%.0f MB written outside the "
-                        "step's events); inputs %.1f MB" % (flush.numel() / 1e6, in_bytes / 1e6))},
-            "ns_chain": {"ms_per_step": ns_ms, "tflops": flops / (ns_ms / 1e3) / 1e12,
-                         "frac": flops / (ns_ms / 1e3) / 1e12 / peaks["bf16_tflops"]},
-            "traced_ms_per_step": traced_ms,
-            "kernels": {k: {"ms_per_step": v["ms"] / args.steps, "launches_per_step":
-                            v["n"] / args.steps} for k, v in kinds.items()},
-            "elementwise": elementwise,
-            "adam": adam,
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clock,
+            "config": {"workload": wl.name, "matrices": wl.n_matrices, "groups": head["groups"],
+                       "counted_gflop_per_step": head["counted_gflop_per_step"],
+                       "graph": head["graph"], "l2": head["l2"]},
+            "ns_chain": head["ns_chain"], "traced_ms_per_step": head["traced_ms_per_step"],
+            "kernels": head["kernels"], "elementwise": head["elementwise"], "adam": adam,
+            "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": head["gpu_launches"], "clocks": head["clocks"],
+            "peaks": {k: peaks[k] for k in ("bf16_tflops", "bf16_tflops_sustained", "hbm_gbs",
+                                            "source")},
+            "configs": configs or None,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -546,6 +648,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--graph", type=int, default=1, help="replay the step as a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time only --workload (no `configs` object)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
