@@ -220,12 +220,21 @@ __device__ bool produce_tile(const TileCtx& T, uint8_t* smem, uint64_t* full, ui
 }
 
 // Before exit: the pair's MMAs have released every armed stage, so its copies
-// landed and no commit arrival can still be on its way to this CTA.
+// landed and no commit arrival can still be on its way to this CTA.  After a
+// failure those releases may never come; the copies themselves land within
+// microseconds, so all stages share one bounded window (not one each).
 __device__ void drain_producer(const ProdState& ps, uint64_t* empty, const Abort& ab) {
-  for (int s = 0; s < Cfg::kStages; ++s)
-    if (ps.armed & (1u << s))
-      if (!ptx::mbar_wait(&empty[s], (ps.armed_parity >> s) & 1u, nullptr))
-        record_failure(ab, kErrTimeoutDrain);
+  const uint64_t t0 = ptx::globaltimer();
+  for (int s = 0; s < Cfg::kStages; ++s) {
+    if (!(ps.armed & (1u << s))) continue;
+    const uint64_t spent = ptx::globaltimer() - t0;
+    if (spent >= ptx::kWaitTimeoutNs ||
+        !ptx::mbar_wait(&empty[s], (ps.armed_parity >> s) & 1u, nullptr, nullptr,
+                        ptx::kWaitTimeoutNs - spent)) {
+      record_failure(ab, kErrTimeoutDrain);
+      return;
+    }
+  }
 }
 
 // ------------------------------------------------------------ MMA issuer
