@@ -120,7 +120,7 @@ muon_status muon_ns5(const void* G, int g_dtype, void* out_bf16,
  * One Muon step on a stack of same-shape weights ([MCS] 四, [PG] 核心思想/分布式细节):
  *   buf <- buf + (1 - momentum) (g - buf)
  *   u   <- g + momentum (buf - g)  if nesterov, else buf
- *   O   <- NS(u) as in muon_ns5 (kept in fp32 for the update)
+ *   O   <- NS(u) as in muon_ns5 (bf16, as the last Newton-Schulz update writes it)
  *   p   <- (1 - lr weight_decay) p - lr s O,   s = lr_scale > 0 ? lr_scale
  *                                                 : max(1, rows/cols)^0.5
  * momentum in [0, 1]; steps in 1..16; eps >= 0; all scalars finite.
