@@ -150,6 +150,10 @@ class ClockSampler:
 # group's stored count ("extrapolated").
 ORACLE_FULL_MAX_FLOPS = 2.0e12
 ORACLE_REPEATS = 3
+# end-to-end leg: untimed pipelined steps, then timed runs of at most E2E_STEPS
+E2E_STEPS = 20
+E2E_WARMUP = 3
+E2E_TRIALS = 3
 
 
 def _oracle_group_inputs(wl, gi, stored, device="cpu"):
@@ -404,7 +408,7 @@ def time_workload(muon, wl, dev, steps, warmup, use_graph, peaks, local, world):
     return res, (tensors, step)
 
 
-def time_e2e(muon, wl, tensors, step, world):
+def time_e2e(muon, wl, tensors, step, world, max_steps=E2E_STEPS):
     """The same grouped step end to end through the public binding with host buffers:
     every step's gradients uploaded from pinned host memory and its parameters read
     back, inside the timed region."""
@@ -416,7 +420,7 @@ def time_e2e(muon, wl, tensors, step, world):
     host_p = [torch.empty(P.shape, dtype=P.dtype, pin_memory=True) for P, _, _ in tensors]
     h2d = sum(t.numel() * t.element_size() for t in host_g)
     d2h = sum(t.numel() * t.element_size() for t in host_p)
-    e2e_steps = 20
+    e2e_steps = max(3, min(E2E_STEPS, max_steps))
     # Three streams, two device gradient buffers and two device parameter
     # snapshots.  Step k's gradient upload (copy stream in) goes into buffer
     # k % 2 once step k-2 is done with it, so it runs beside step k-1; step k
@@ -433,45 +437,57 @@ def time_e2e(muon, wl, tensors, step, world):
     dev_g = [[G for _, G, _ in tensors], grads2]
     steps_ab = [step, step2]
     snap = [[torch.empty_like(P) for P, _, _ in tensors] for _ in range(2)]
-    ev_in = [torch.cuda.Event() for _ in range(e2e_steps)]
-    ev_done = [torch.cuda.Event() for _ in range(e2e_steps)]
-    ev_out = [torch.cuda.Event() for _ in range(e2e_steps)]
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    barrier(world)
-    t0 = time.perf_counter()
-    e0.record(stream)
-    for k in range(e2e_steps):
-        up.wait_event(ev_done[k - 2] if k > 1 else e0)
-        with torch.cuda.stream(up):
-            for G, hg in zip(dev_g[k % 2], host_g):
-                G.copy_(hg, non_blocking=True)
-            ev_in[k].record(up)
-        stream.wait_event(ev_in[k])
-        steps_ab[k % 2]()
-        if k > 1:
-            stream.wait_event(ev_out[k - 2])
-        for (P, _, _), sp in zip(tensors, snap[k % 2]):
-            sp.copy_(P, non_blocking=True)
-        ev_done[k].record(stream)
-        down.wait_event(ev_done[k])
-        with torch.cuda.stream(down):
-            for sp, hp in zip(snap[k % 2], host_p):
-                hp.copy_(sp, non_blocking=True)
-            ev_out[k].record(down)
-    stream.wait_event(ev_out[e2e_steps - 1])
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_ms = max(e0.elapsed_time(e1), 1e3 * (time.perf_counter() - t0))
-    e2e_ms, e2e_units = aggregate_over_ranks(e2e_ms, flops * e2e_steps, world)
+    def run(n):
+        """n pipelined steps; returns (device ms, wall ms) for all of them."""
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_done = [torch.cuda.Event() for _ in range(n)]
+        ev_out = [torch.cuda.Event() for _ in range(n)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for k in range(n):
+            up.wait_event(ev_done[k - 2] if k > 1 else e0)
+            with torch.cuda.stream(up):
+                for G, hg in zip(dev_g[k % 2], host_g):
+                    G.copy_(hg, non_blocking=True)
+                ev_in[k].record(up)
+            stream.wait_event(ev_in[k])
+            steps_ab[k % 2]()
+            if k > 1:
+                stream.wait_event(ev_out[k - 2])
+            for (P, _, _), sp in zip(tensors, snap[k % 2]):
+                sp.copy_(P, non_blocking=True)
+            ev_done[k].record(stream)
+            down.wait_event(ev_done[k])
+            with torch.cuda.stream(down):
+                for sp, hp in zip(snap[k % 2], host_p):
+                    hp.copy_(sp, non_blocking=True)
+                ev_out[k].record(down)
+        stream.wait_event(ev_out[n - 1])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return e0.elapsed_time(e1), 1e3 * (time.perf_counter() - t0)
+
+    run(E2E_WARMUP)  # untimed: the second step object's first calls, first touch of host pages
+    # The host link is shared with the machine's other jobs: three timed runs, the
+    # median reported, all three listed.
+    trials = [run(e2e_steps) for _ in range(E2E_TRIALS)]
+    per_step = sorted(max(dev_ms, wall_ms) / e2e_steps for dev_ms, wall_ms in trials)
+    med = per_step[len(per_step) // 2]
+    dev_ms, wall_ms = next(t for t in trials if max(t) / e2e_steps == med)
+    e2e_ms, e2e_units = aggregate_over_ranks(med * e2e_steps, flops * e2e_steps, world)
     return {"value": e2e_units / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
+            "warmup": E2E_WARMUP, "trials_ms_per_step": per_step,
+            "device_ms_per_step": dev_ms / e2e_steps, "wall_ms_per_step": wall_ms / e2e_steps,
             "schedule": "gradient upload (copy stream, two device gradient buffers) and "
                         "parameter read-back from device snapshots (second copy stream, two "
                         "snapshots) of neighbouring steps overlap the compute; every copy of "
-                        "every step inside the timed region"}
+                        "every step inside the timed region; median of three timed runs"}
 
 
 def run_gpu(args, wl):
@@ -491,7 +507,7 @@ def run_gpu(args, wl):
     head, (tensors, step) = time_workload(muon, wl, dev, args.steps, args.warmup,
                                           bool(args.graph), peaks, local, world)
     adam = time_adam(args, wl, dev, peaks) if wl.adam else None
-    e2e = time_e2e(muon, wl, tensors, step, world)
+    e2e = time_e2e(muon, wl, tensors, step, world, args.steps)
     del tensors, step
     torch.cuda.empty_cache()
 
