@@ -483,7 +483,7 @@ def time_e2e(muon, wl, tensors, step, world, max_steps=E2E_STEPS):
 
     run(E2E_WARMUP)  # untimed: the second step object's first calls, first touch of host pages
     # The host link is shared with the machine's other jobs: E2E_TRIALS timed runs, the
-    # median reported, all three listed.
+    # median reported, all of them listed.
     trials = [run(e2e_steps) for _ in range(E2E_TRIALS)]
     per_step = sorted(max(dev_ms, wall_ms) / e2e_steps for dev_ms, wall_ms in trials)
     med = per_step[len(per_step) // 2]
