@@ -361,16 +361,11 @@ def time_workload(muon, wl, dev, steps, warmup, use_graph, peaks, local, world):
     per_launch_ms = dom["ms"] / dom["n"]
     if dom["flops"] > 0:
         achieved = dom["flops"] / dom["n"] / (per_launch_ms / 1e3) / 1e12
-        # the burst peak for a kernel in a short step; the sustained one (the
-        # long loop under the power cap) inside a long step, or once the power
-        # cap showed in the timed region
-        sustained = (ms / steps >= LONG_STEP_MS or "sw_power_cap" in clock.get("reasons", [])) \
-            and peaks.get("bf16_tflops_sustained")
-        peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+        peak, which = tensor_peak(ms / steps, clock.get("reasons", []), peaks)
         roof = {"kernel": dom_name, "bound": "tensor", "achieved": achieved,
                 "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic_for(dom_name, wl.name),
-                "peak_source": f"{peaks['source']} {'sustained' if sustained else 'burst'} bf16",
+                "peak_source": f"{peaks['source']} {which} bf16",
                 "frac_of_burst": achieved / peaks["bf16_tflops"], "ms_per_launch": per_launch_ms,
                 "flops_per_launch": dom["flops"] / dom["n"]}
     else:
@@ -416,6 +411,23 @@ def time_workload(muon, wl, dev, steps, warmup, use_graph, peaks, local, world):
         "elementwise": elementwise, "roofline": roof, "gpu_launches": launches, "clocks": clock,
     }
     return res, (tensors, step)
+
+
+def tensor_peak(step_ms, reasons, peaks):
+    """The bf16 peak a tensor-core kernel is measured against: the burst figure in a
+    short step, the sustained one (the long loop under the power cap) in a step of
+    LONG_STEP_MS or more or once the power cap showed in the timed region."""
+    if step_ms >= LONG_STEP_MS or "sw_power_cap" in reasons:
+        return peaks["bf16_tflops_sustained"], "sustained"
+    return peaks["bf16_tflops"], "burst"
+
+
+def median_trial(trials, steps):
+    """(every trial's ms per step, sorted; the (device ms, wall ms) of the median trial),
+    a trial's time per step being the longer of its device and wall clocks."""
+    per_step = sorted(max(t) / steps for t in trials)
+    med = per_step[len(per_step) // 2]
+    return per_step, next(t for t in trials if max(t) / steps == med)
 
 
 def time_e2e(muon, wl, tensors, step, world, max_steps=E2E_STEPS):
@@ -485,9 +497,8 @@ def time_e2e(muon, wl, tensors, step, world, max_steps=E2E_STEPS):
     # The host link is shared with the machine's other jobs: E2E_TRIALS timed runs, the
     # median reported, all of them listed.
     trials = [run(e2e_steps) for _ in range(E2E_TRIALS)]
-    per_step = sorted(max(dev_ms, wall_ms) / e2e_steps for dev_ms, wall_ms in trials)
-    med = per_step[len(per_step) // 2]
-    dev_ms, wall_ms = next(t for t in trials if max(t) / e2e_steps == med)
+    per_step, (dev_ms, wall_ms) = median_trial(trials, e2e_steps)
+    med = max(dev_ms, wall_ms) / e2e_steps
     e2e_ms, e2e_units = aggregate_over_ranks(med * e2e_steps, flops * e2e_steps, world)
     return {"value": e2e_units / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
